@@ -1,0 +1,244 @@
+"""fp64 CPU oracle for the tensor-parallel Transformer MLP block.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(the CUDA library and its Python binding) never imports it, and it never
+imports the product path.
+
+The arithmetic lives in ``oracle.c`` (plain fp64 loops, OpenMP over output
+rows); this module only compiles it with the host C compiler, converts arrays
+to contiguous float64 and passes pointers.  The sequence-parallel helpers
+concatenate and split along the token dimension, which is the definition of
+the sequence-parallel gather / reduce-scatter ("并行训练范式 / 序列并行" on
+"Megatron-LM：NVIDIA 的大规模并行训练方案").
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_dpp = ctypes.POINTER(_dp)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so with the host C compiler."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _configure(lib):
+    lib.oracle_gelu.restype = ctypes.c_double
+    lib.oracle_gelu.argtypes = [ctypes.c_double]
+    lib.oracle_gelu_grad.restype = ctypes.c_double
+    lib.oracle_gelu_grad.argtypes = [ctypes.c_double]
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_get_threads.restype = ctypes.c_int
+    dims = [_i64, _i64, _i64, ctypes.c_int]
+    lib.oracle_forward.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp, _dpp, _dpp, _dp]
+    lib.oracle_backward.argtypes = dims + [_dp, _dpp, _dpp, _dpp, _dpp, _dp,
+                                           _dpp, _dp, _dpp, _dp, _dpp, _dp]
+    lib.oracle_rows.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp, _dp,
+                                       _i64, ctypes.POINTER(_i64), _dp, _dp]
+    lib.oracle_cols.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp,
+                                       _i64, ctypes.POINTER(_i64), _dp, _dp, _dp]
+    lib.oracle_db2.argtypes = [_i64, _i64, _dp, _dp]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _configure(ctypes.CDLL(build()))
+        return _lib
+
+
+@contextlib.contextmanager
+def _library(path: str):
+    """Route every call through another build of oracle.c for the duration of
+    the block (the planted-mistake test compiles mutated copies)."""
+    global _lib
+    _load()
+    with _lock:
+        saved, _lib = _lib, _configure(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def _f64(a) -> np.ndarray:
+    """Contiguous float64 copy/view of an array-like (torch tensors included)."""
+    if hasattr(a, "detach"):  # torch tensor: exact upcast on the host
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _ptrs(arrs):
+    arr = (_dp * len(arrs))(*[_ptr(a) for a in arrs])
+    return ctypes.cast(arr, _dpp), arr
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def gelu(x: float) -> float:
+    return float(_load().oracle_gelu(float(x)))
+
+
+def gelu_grad(x: float) -> float:
+    return float(_load().oracle_gelu_grad(float(x)))
+
+
+def _check_shards(X, A, b1, B, b2):
+    t = len(A)
+    if t < 1 or len(B) != t:
+        raise ValueError("A and B must hold the same number (>=1) of shards")
+    T, h = X.shape
+    fi = A[0].shape[1]
+    for a, b in zip(A, B):
+        if a.shape != (h, fi) or b.shape != (fi, h):
+            raise ValueError("shard shapes must be A_i [h, f/t] and B_i [f/t, h]")
+    if b1.shape != (t * fi,) or b2.shape != (h,):
+        raise ValueError("b1 must be [f], b2 must be [h]")
+    return T, h, t * fi, t, fi
+
+
+def forward(X, A_shards, b1, B_shards, b2):
+    """Z = (sum_i GeLU(X.A_i + b1_i).B_i) + b2.  Returns dict Y, H (lists of
+    [T, f/t] shards) and Z [T, h], all float64."""
+    lib = _load()
+    X = _f64(X); b1 = _f64(b1); b2 = _f64(b2)
+    A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
+    T, h, f, t, fi = _check_shards(X, A, b1, B, b2)
+    Y = [np.empty((T, fi)) for _ in range(t)]
+    H = [np.empty((T, fi)) for _ in range(t)]
+    Z = np.empty((T, h))
+    pA, _ka = _ptrs(A); pB, _kb = _ptrs(B); pY, _ky = _ptrs(Y); pH, _kh = _ptrs(H)
+    lib.oracle_forward(T, h, f, t, _ptr(X), pA, _ptr(b1), pB, _ptr(b2), pY, pH, _ptr(Z))
+    return {"Y": Y, "H": H, "Z": Z}
+
+
+def backward(X, A_shards, B_shards, Y, H, dZ):
+    """Chain rule of :func:`forward` for upstream gradient dZ.  Returns dict
+    dY (list), dX, dA (list of [h, f/t]), db1 [f], dB (list of [f/t, h]), db2 [h]."""
+    lib = _load()
+    X = _f64(X); dZ = _f64(dZ)
+    A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
+    Y = [_f64(y) for y in Y]; H = [_f64(x) for x in H]
+    t = len(A); T, h = X.shape; fi = A[0].shape[1]; f = t * fi
+    dY = [np.empty((T, fi)) for _ in range(t)]
+    dX = np.empty((T, h))
+    dA = [np.empty((h, fi)) for _ in range(t)]
+    dB = [np.empty((fi, h)) for _ in range(t)]
+    db1 = np.empty(f); db2 = np.empty(h)
+    keep = []
+    def P(lst):
+        p, k = _ptrs(lst); keep.append(k); return p
+    lib.oracle_backward(T, h, f, t, _ptr(X), P(A), P(B), P(Y), P(H), _ptr(dZ),
+                        P(dY), _ptr(dX), P(dA), _ptr(db1), P(dB), _ptr(db2))
+    return {"dY": dY, "dX": dX, "dA": dA, "db1": db1, "dB": dB, "db2": db2}
+
+
+def forward_backward(X, A_shards, b1, B_shards, b2, dZ):
+    fw = forward(X, A_shards, b1, B_shards, b2)
+    bw = backward(X, A_shards, B_shards, fw["Y"], fw["H"], dZ)
+    return {**fw, **bw}
+
+
+def rows(X, A_shards, b1, B_shards, b2, dZ, row_idx):
+    """Z[r, :] and dX[r, :] for the selected token rows only."""
+    lib = _load()
+    X = _f64(X); dZ = _f64(dZ); b1 = _f64(b1); b2 = _f64(b2)
+    A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
+    T, h, f, t, fi = _check_shards(X, A, b1, B, b2)
+    idx = np.ascontiguousarray(np.asarray(row_idx, dtype=np.int64))
+    if idx.size and (idx.min() < 0 or idx.max() >= T):
+        raise IndexError("row index out of range")
+    Zr = np.empty((idx.size, h)); dXr = np.empty((idx.size, h))
+    pA, _ka = _ptrs(A); pB, _kb = _ptrs(B)
+    lib.oracle_rows(T, h, f, t, _ptr(X), pA, _ptr(b1), pB, _ptr(b2), _ptr(dZ),
+                    idx.size, idx.ctypes.data_as(ctypes.POINTER(_i64)), _ptr(Zr), _ptr(dXr))
+    return {"Z": Zr, "dX": dXr}
+
+
+def cols(X, A_shards, b1, B_shards, dZ, col_idx):
+    """dA[:, c], dB[c, :] and db1[c] for the selected global ffn columns c."""
+    lib = _load()
+    X = _f64(X); dZ = _f64(dZ); b1 = _f64(b1)
+    A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
+    t = len(A); T, h = X.shape; fi = A[0].shape[1]; f = t * fi
+    idx = np.ascontiguousarray(np.asarray(col_idx, dtype=np.int64))
+    if idx.size and (idx.min() < 0 or idx.max() >= f):
+        raise IndexError("column index out of range")
+    dAc = np.empty((idx.size, h)); dBc = np.empty((idx.size, h)); db1c = np.empty(idx.size)
+    pA, _ka = _ptrs(A); pB, _kb = _ptrs(B)
+    lib.oracle_cols(T, h, f, t, _ptr(X), pA, _ptr(b1), pB, _ptr(dZ),
+                    idx.size, idx.ctypes.data_as(ctypes.POINTER(_i64)),
+                    _ptr(dAc), _ptr(dBc), _ptr(db1c))
+    return {"dA_cols": dAc, "dB_rows": dBc, "db1": db1c}
+
+
+def db2(dZ):
+    lib = _load()
+    dZ = _f64(dZ)
+    T, h = dZ.shape
+    out = np.empty(h)
+    lib.oracle_db2(T, h, _ptr(dZ), _ptr(out))
+    return out
+
+
+# ---- sequence-parallel variant ----------------------------------------------
+# The sequence-parallel block takes X and dZ as seq_chunks token chunks and
+# returns Z and dX in the same chunking: gather = concatenation along tokens
+# before the column-parallel linear, reduce-scatter = the shard sum followed by
+# a split along tokens after the row-parallel linear.
+
+def sp_gather(chunks):
+    return np.concatenate([_f64(c) for c in chunks], axis=0)
+
+
+def sp_scatter(full, n):
+    T = full.shape[0]
+    if T % n:
+        raise ValueError("token count must divide evenly into chunks")
+    return [np.ascontiguousarray(x) for x in np.split(full, n, axis=0)]
+
+
+def forward_backward_sp(X_chunks, A_shards, b1, B_shards, b2, dZ_chunks):
+    n = len(X_chunks)
+    out = forward_backward(sp_gather(X_chunks), A_shards, b1, B_shards, b2, sp_gather(dZ_chunks))
+    out["Z_chunks"] = sp_scatter(out["Z"], n)
+    out["dX_chunks"] = sp_scatter(out["dX"], n)
+    return out

@@ -1,0 +1,324 @@
+/*
+ * oracle.c -- fp64 CPU oracle for the tensor-parallel Transformer MLP block
+ *
+ *     Z = GeLU(X.A + b1).B + b2,  A split by columns into t shards, B by rows.
+ *
+ * TEST INFRASTRUCTURE.  This file is the slow, obviously correct definition
+ * the CUDA path is checked against.  Only the test suite, the smoke check and
+ * the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA library, and it never calls into it.
+ *
+ * Sources (page title, section):
+ *   [FGO]  "Megatron-LM：NVIDIA 的大规模并行训练方案" (freeguideonline.com),
+ *          section "Megatron-LM 核心架构 / 张量并行原理" (column split,
+ *          row split, MLP = column then row) and "融合优化技术" (Bias+GeLU).
+ *   [CH2]  "2、分布式训练基础：数据并行、模型并行、流水线并行的基本概念与区别",
+ *          section "2.2 模型并行 —— 张量并行 / 核心原理" (Y = XW, column and
+ *          row parallel linear layers).
+ *   [FGO-SP] same page as [FGO], section "并行训练范式 / 序列并行".
+ *
+ * Everything is fp64.  Inputs are whatever values the caller passes (the
+ * tests pass the exact bf16 values upcast to double).  Matrices are dense
+ * row-major.  Shard i of A is the column block A[:, i*fi:(i+1)*fi] stored as
+ * its own [h, fi] array; shard i of B is the row block B[i*fi:(i+1)*fi, :]
+ * stored as its own [fi, h] array; fi = f / t.
+ *
+ * Readings where the pages are silent (each one is listed in the design
+ * notes):
+ *   - "GeLU" is the tanh form of Hendrycks & Gimpel (2016):
+ *       GeLU(x) = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))).
+ *   - b2 is added once, after the shard partial products are summed (after
+ *     the row-parallel "AllReduce" of [FGO]/[CH2]); b1 is one [f] vector whose
+ *     slice [i*fi, (i+1)*fi) belongs to shard i.
+ *   - The backward pass is the chain rule of this forward pass (the pages do
+ *     not write it down): with dZ = dL/dZ,
+ *       dH_i = dZ.B_i^T, dY_i = dH_i * GeLU'(Y_i), dX = sum_i dY_i.A_i^T,
+ *       dA_i = X^T.dY_i, dB_i = H_i^T.dZ, db1 = column sums of dY,
+ *       db2 = column sums of dZ.
+ *
+ * Parallelism: OpenMP over output rows only; every output element is a
+ * plain sum taken in index order.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- threads ----------------------------------------------------------- */
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_get_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---- GeLU, tanh form ----------------------------------------------------
+ * u(x) = sqrt(2/pi) * (x + 0.044715 x^3)
+ * GeLU(x)  = 0.5 x (1 + tanh u)
+ * GeLU'(x) = 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) du/dx,
+ *            du/dx = sqrt(2/pi) * (1 + 3 * 0.044715 x^2)
+ */
+static double gelu_k0(void) { return sqrt(2.0 / acos(-1.0)); }
+static const double GELU_K1 = 0.044715;
+
+double oracle_gelu(double x) {
+    double u = gelu_k0() * (x + GELU_K1 * x * x * x);
+    return 0.5 * x * (1.0 + tanh(u));
+}
+
+double oracle_gelu_grad(double x) {
+    double k0 = gelu_k0();
+    double u = k0 * (x + GELU_K1 * x * x * x);
+    double th = tanh(u);
+    double du = k0 * (1.0 + 3.0 * GELU_K1 * x * x);
+    return 0.5 * (1.0 + th) + 0.5 * x * (1.0 - th * th) * du;
+}
+
+/* ---- forward ------------------------------------------------------------
+ * Column-parallel first linear ([CH2] 2.2 column split, [FGO] 张量并行原理):
+ *   for each shard i:  Y_i = X.A_i + b1[i*fi:(i+1)*fi],  H_i = GeLU(Y_i)
+ *   (bias and GeLU applied together, [FGO] 融合优化技术)
+ * Row-parallel second linear ([CH2] 2.2 row split):
+ *   Z = (sum_i H_i.B_i) + b2
+ * Outputs: Y[i], H[i] are [T, fi]; Z is [T, h].
+ */
+void oracle_forward(int64_t T, int64_t h, int64_t f, int t,
+                    const double *X,
+                    const double *const *A, const double *b1,
+                    const double *const *B, const double *b2,
+                    double *const *Y, double *const *H, double *Z) {
+    const int64_t fi = f / t;
+    for (int i = 0; i < t; ++i) {
+        const double *Ai = A[i];
+        double *Yi = Y[i], *Hi = H[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < T; ++r) {
+            double *yrow = Yi + r * fi;
+            for (int64_t j = 0; j < fi; ++j) yrow[j] = 0.0;
+            for (int64_t k = 0; k < h; ++k) {
+                const double x = X[r * h + k];
+                const double *arow = Ai + k * fi;
+                for (int64_t j = 0; j < fi; ++j) yrow[j] += x * arow[j];
+            }
+            for (int64_t j = 0; j < fi; ++j) {
+                yrow[j] += b1[i * fi + j];
+                Hi[r * fi + j] = oracle_gelu(yrow[j]);
+            }
+        }
+    }
+    /* row-parallel partial products, summed over shards (the on-chip stand-in
+     * for the AllReduce), then the bias once */
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        double *zrow = Z + r * h;
+        for (int64_t n = 0; n < h; ++n) zrow[n] = 0.0;
+        for (int i = 0; i < t; ++i) {
+            const double *Hi = H[i], *Bi = B[i];
+            for (int64_t j = 0; j < fi; ++j) {
+                const double hv = Hi[r * fi + j];
+                const double *brow = Bi + j * h;
+                for (int64_t n = 0; n < h; ++n) zrow[n] += hv * brow[n];
+            }
+        }
+        for (int64_t n = 0; n < h; ++n) zrow[n] += b2[n];
+    }
+}
+
+/* ---- backward -----------------------------------------------------------
+ * Chain rule of oracle_forward for upstream gradient dZ = dL/dZ [T, h]:
+ *   dH_i = dZ.B_i^T                   [T, fi]
+ *   dY_i = dH_i * GeLU'(Y_i)          [T, fi]   (written to dY[i])
+ *   dX   = sum_i dY_i.A_i^T           [T, h]    (sum over shards, as the
+ *                                                 backward AllReduce)
+ *   dA_i = X^T.dY_i                   [h, fi]
+ *   dB_i = H_i^T.dZ                   [fi, h]
+ *   db1[i*fi + j] = sum_r dY_i[r, j]  [f]
+ *   db2[n] = sum_r dZ[r, n]           [h]
+ */
+void oracle_backward(int64_t T, int64_t h, int64_t f, int t,
+                     const double *X,
+                     const double *const *A, const double *const *B,
+                     const double *const *Y, const double *const *H,
+                     const double *dZ,
+                     double *const *dY, double *dX,
+                     double *const *dA, double *db1,
+                     double *const *dB, double *db2) {
+    const int64_t fi = f / t;
+    /* dY_i */
+    for (int i = 0; i < t; ++i) {
+        const double *Bi = B[i], *Yi = Y[i];
+        double *dYi = dY[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < T; ++r) {
+            for (int64_t j = 0; j < fi; ++j) {
+                double dh = 0.0;
+                const double *brow = Bi + j * h;
+                for (int64_t n = 0; n < h; ++n) dh += dZ[r * h + n] * brow[n];
+                dYi[r * fi + j] = dh * oracle_gelu_grad(Yi[r * fi + j]);
+            }
+        }
+    }
+    /* dX = sum_i dY_i.A_i^T */
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        for (int64_t k = 0; k < h; ++k) {
+            double acc = 0.0;
+            for (int i = 0; i < t; ++i) {
+                const double *arow = A[i] + k * fi;
+                const double *dyrow = dY[i] + r * fi;
+                for (int64_t j = 0; j < fi; ++j) acc += dyrow[j] * arow[j];
+            }
+            dX[r * h + k] = acc;
+        }
+    }
+    /* dA_i = X^T.dY_i */
+    for (int i = 0; i < t; ++i) {
+        const double *dYi = dY[i];
+        double *dAi = dA[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t k = 0; k < h; ++k) {
+            double *out = dAi + k * fi;
+            for (int64_t j = 0; j < fi; ++j) out[j] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                const double x = X[r * h + k];
+                const double *dyrow = dYi + r * fi;
+                for (int64_t j = 0; j < fi; ++j) out[j] += x * dyrow[j];
+            }
+        }
+    }
+    /* dB_i = H_i^T.dZ */
+    for (int i = 0; i < t; ++i) {
+        const double *Hi = H[i];
+        double *dBi = dB[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < fi; ++j) {
+            double *out = dBi + j * h;
+            for (int64_t n = 0; n < h; ++n) out[n] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                const double hv = Hi[r * fi + j];
+                const double *dzrow = dZ + r * h;
+                for (int64_t n = 0; n < h; ++n) out[n] += hv * dzrow[n];
+            }
+        }
+    }
+    /* db1: column sums of dY, shard by shard */
+    for (int i = 0; i < t; ++i) {
+        const double *dYi = dY[i];
+        for (int64_t j = 0; j < fi; ++j) {
+            double s = 0.0;
+            for (int64_t r = 0; r < T; ++r) s += dYi[r * fi + j];
+            db1[i * fi + j] = s;
+        }
+    }
+    /* db2: column sums of dZ */
+    for (int64_t n = 0; n < h; ++n) {
+        double s = 0.0;
+        for (int64_t r = 0; r < T; ++r) s += dZ[r * h + n];
+        db2[n] = s;
+    }
+}
+
+/* ---- sampled outputs ----------------------------------------------------
+ * The same definitions as above, evaluated only for selected outputs, so a
+ * full-size problem can be checked one output at a time.
+ *
+ * oracle_rows: for each selected token row r = rows[q]:
+ *   Zr[q, :]  = Z[r, :]   and   dXr[q, :] = dX[r, :]
+ * (needs row r of Y_i, H_i and dY_i for every shard, computed here).
+ */
+void oracle_rows(int64_t T, int64_t h, int64_t f, int t,
+                 const double *X,
+                 const double *const *A, const double *b1,
+                 const double *const *B, const double *b2,
+                 const double *dZ,
+                 int64_t nrows, const int64_t *rows,
+                 double *Zr, double *dXr) {
+    const int64_t fi = f / t;
+    (void)T;
+    #pragma omp parallel for schedule(dynamic)
+    for (int64_t q = 0; q < nrows; ++q) {
+        const int64_t r = rows[q];
+        double *z = Zr + q * h;
+        double *dx = dXr + q * h;
+        for (int64_t n = 0; n < h; ++n) { z[n] = 0.0; dx[n] = 0.0; }
+        for (int i = 0; i < t; ++i) {
+            const double *Ai = A[i], *Bi = B[i];
+            for (int64_t j = 0; j < fi; ++j) {
+                double y = 0.0;
+                for (int64_t k = 0; k < h; ++k) y += X[r * h + k] * Ai[k * fi + j];
+                y += b1[i * fi + j];
+                const double hv = oracle_gelu(y);
+                double dh = 0.0;
+                for (int64_t n = 0; n < h; ++n) dh += dZ[r * h + n] * Bi[j * h + n];
+                const double dy = dh * oracle_gelu_grad(y);
+                for (int64_t n = 0; n < h; ++n) z[n] += hv * Bi[j * h + n];
+                for (int64_t k = 0; k < h; ++k) dx[k] += dy * Ai[k * fi + j];
+            }
+        }
+        for (int64_t n = 0; n < h; ++n) z[n] += b2[n];
+    }
+}
+
+/* oracle_cols: for each selected ffn column c = cols[q] (global index in
+ * [0, f), shard i = c / fi, local column j = c % fi):
+ *   dAc[q, :] = dA_i[:, j]   (length h)
+ *   dBc[q, :] = dB_i[j, :]   (length h)
+ *   db1c[q]   = db1[c]
+ * (needs column j of Y_i, H_i and dY_i over all T rows, computed here).
+ */
+void oracle_cols(int64_t T, int64_t h, int64_t f, int t,
+                 const double *X,
+                 const double *const *A, const double *b1,
+                 const double *const *B,
+                 const double *dZ,
+                 int64_t ncols, const int64_t *cols,
+                 double *dAc, double *dBc, double *db1c) {
+    const int64_t fi = f / t;
+    #pragma omp parallel for schedule(dynamic)
+    for (int64_t q = 0; q < ncols; ++q) {
+        const int64_t c = cols[q];
+        const int i = (int)(c / fi);
+        const int64_t j = c % fi;
+        const double *Ai = A[i], *Bi = B[i];
+        double *da = dAc + q * h;
+        double *db = dBc + q * h;
+        double s1 = 0.0;
+        for (int64_t n = 0; n < h; ++n) { da[n] = 0.0; db[n] = 0.0; }
+        for (int64_t r = 0; r < T; ++r) {
+            double y = 0.0;
+            for (int64_t k = 0; k < h; ++k) y += X[r * h + k] * Ai[k * fi + j];
+            y += b1[c];
+            const double hv = oracle_gelu(y);
+            double dh = 0.0;
+            for (int64_t n = 0; n < h; ++n) dh += dZ[r * h + n] * Bi[j * h + n];
+            const double dy = dh * oracle_gelu_grad(y);
+            for (int64_t k = 0; k < h; ++k) da[k] += X[r * h + k] * dy;
+            for (int64_t n = 0; n < h; ++n) db[n] += hv * dZ[r * h + n];
+            s1 += dy;
+        }
+        db1c[q] = s1;
+    }
+}
+
+/* db2 alone (column sums of dZ), for full-size problems. */
+void oracle_db2(int64_t T, int64_t h, const double *dZ, double *db2) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < h; ++n) {
+        double s = 0.0;
+        for (int64_t r = 0; r < T; ++r) s += dZ[r * h + n];
+        db2[n] = s;
+    }
+}

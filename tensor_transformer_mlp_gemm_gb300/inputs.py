@@ -1,0 +1,113 @@
+"""Seeded synthetic inputs for the tensor-parallel MLP block.
+
+This module is shared by the CUDA path's tests/benchmark and by the oracle's
+tests.  It draws random numbers and lays them out (shards, sequence chunks);
+it holds none of the block's arithmetic.
+
+Recipe (every workload): a CPU ``torch.Generator`` seeded with ``seed`` draws,
+in this order, X [T, h], A [h, f], b1 [f], B [f, h], b2 [h], dZ [T, h] with
+``torch.randn`` in fp32; each draw is multiplied by its standard deviation and
+rounded to bf16 (round to nearest even).  X and dZ have std 1, the weights
+``sigma_w``, the biases 0.02.
+
+Token rows are ordered sequence-major ([seq, micro-batch] flattened, the usual
+[s, b, h] activation layout), so sequence chunk j is the contiguous row range
+[j*T/n, (j+1)*T/n): a span of sequence positions for every sample.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    micro_batch: int
+    seq: int
+    hidden: int          # h
+    ffn: int             # f
+    t: int               # tensor-parallel shards
+    sigma_w: float       # weight std
+    seq_chunks: int = 1  # sequence-parallel chunks (1 = off, else t)
+    sigma_b: float = 0.02
+
+    @property
+    def tokens(self) -> int:
+        return self.micro_batch * self.seq
+
+    @property
+    def flops(self) -> int:
+        """fwd+bwd FLOPs: six GEMMs of 2*T*h*f each."""
+        return 12 * self.tokens * self.hidden * self.ffn
+
+    def with_tokens(self, tokens: int) -> "Workload":
+        """Same layer with a different token count (micro_batch=1, seq=tokens)."""
+        return replace(self, name=f"{self.name}[T={tokens}]", micro_batch=1, seq=tokens,
+                       seq_chunks=1)
+
+
+# The five workloads: shapes and distributions of the pages' 1.3B-class and
+# 175B-class examples plus a tiny and a small case and the sequence-parallel one.
+WORKLOADS = {
+    "tiny": Workload("tiny", 2, 64, 256, 1024, 2, 0.02),
+    "small_gpt": Workload("small_gpt", 4, 1024, 1024, 4096, 2, 0.02),
+    "gpt_1p3b_t1": Workload("gpt_1p3b_t1", 4, 1024, 2048, 8192, 1, 0.02),
+    "gpt_1p3b_t4": Workload("gpt_1p3b_t4", 4, 1024, 2048, 8192, 4, 0.02),
+    "gpt_175b": Workload("gpt_175b", 1, 2048, 12288, 49152, 8, 0.006),
+    "sp_h4096": Workload("sp_h4096", 8, 2048, 4096, 16384, 8, 0.02, seq_chunks=8),
+}
+
+
+def custom(tokens: int, hidden: int, ffn: int, t: int, sigma_w: float = 0.02,
+           seq_chunks: int = 1, name: str = "custom") -> Workload:
+    return Workload(name, 1, tokens, hidden, ffn, t, sigma_w, seq_chunks)
+
+
+def make_inputs(w: Workload, seed: int = 0) -> dict:
+    """Full (unsharded) bf16 CPU tensors X, A, b1, B, b2, dZ for workload w."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    T, h, f = w.tokens, w.hidden, w.ffn
+
+    def draw(shape, std):
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(torch.bfloat16)
+
+    X = draw((T, h), 1.0)
+    A = draw((h, f), w.sigma_w)
+    b1 = draw((f,), w.sigma_b)
+    B = draw((f, h), w.sigma_w)
+    b2 = draw((h,), w.sigma_b)
+    dZ = draw((T, h), 1.0)
+    return {"X": X, "A": A, "b1": b1, "B": B, "b2": b2, "dZ": dZ}
+
+
+def column_shards(A: torch.Tensor, t: int) -> list:
+    """A [h, f] -> t contiguous column blocks [h, f/t] (own allocations)."""
+    f = A.shape[1]
+    if f % t:
+        raise ValueError("f must be divisible by t")
+    fi = f // t
+    return [A[:, i * fi:(i + 1) * fi].contiguous() for i in range(t)]
+
+
+def row_shards(B: torch.Tensor, t: int) -> list:
+    """B [f, h] -> t contiguous row blocks [f/t, h] (own allocations)."""
+    f = B.shape[0]
+    if f % t:
+        raise ValueError("f must be divisible by t")
+    fi = f // t
+    return [B[i * fi:(i + 1) * fi, :].contiguous() for i in range(t)]
+
+
+def seq_chunks(X: torch.Tensor, n: int) -> list:
+    """X [T, h] -> n contiguous token chunks [T/n, h] (own allocations)."""
+    T = X.shape[0]
+    if T % n:
+        raise ValueError("T must be divisible by the number of chunks")
+    r = T // n
+    return [X[j * r:(j + 1) * r, :].contiguous() for j in range(n)]

@@ -1,0 +1,58 @@
+"""Planted mistakes: each mutation of oracle.c (a dropped term, a wrong sign,
+a wrong index, a transposed operand) must make at least one independent pin
+in test_oracle_pins.py fail.  The mutants are compiled and run on the CPU."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, original text, mutated text); each original occurs exactly once
+MUTATIONS = [
+    ("b2 added twice", "zrow[n] += b2[n];", "zrow[n] += 2.0 * b2[n];"),
+    ("b1 slice of shard 0 for every shard", "yrow[j] += b1[i * fi + j];", "yrow[j] += b1[j];"),
+    ("GeLU' sign", "0.5 * x * (1.0 - th * th) * du", "0.5 * x * (1.0 + th * th) * du"),
+    ("GeLU' dropped factor 3", "(1.0 + 3.0 * GELU_K1 * x * x)", "(1.0 + GELU_K1 * x * x)"),
+    ("GeLU sign of tanh", "return 0.5 * x * (1.0 + tanh(u));", "return 0.5 * x * (1.0 - tanh(u));"),
+    ("dX drops last shard", "            for (int i = 0; i < t; ++i) {\n                const double *arow",
+     "            for (int i = 0; i + 1 < t; ++i) {\n                const double *arow"),
+    ("dX transposed weight index", "const double *arow = A[i] + k * fi;",
+     "const double *arow = A[i] + (k % fi) * fi;"),
+    ("dB from Y instead of H", "const double *Hi = H[i];\n        double *dBi", "const double *Hi = Y[i];\n        double *dBi"),
+    ("dA drops first token", "for (int64_t r = 0; r < T; ++r) {\n                const double x = X[r * h + k];",
+     "for (int64_t r = 1; r < T; ++r) {\n                const double x = X[r * h + k];"),
+    ("db1 sign", "db1[i * fi + j] = s;", "db1[i * fi + j] = -s;"),
+    ("dH uses dZ transposed", "for (int64_t n = 0; n < h; ++n) dh += dZ[r * h + n] * brow[n];\n                dYi",
+     "for (int64_t n = 0; n < h; ++n) dh += dZ[(n % T) * h + (r % h)] * brow[n];\n                dYi"),
+]
+
+PIN_CALLS = [
+    lambda: pins.test_exact_saturated_random(3, 4, 8, 2),
+    lambda: pins.test_exact_saturated_random(4, 8, 16, 4),
+    lambda: pins.test_random_block_against_numpy(7, 5, 12, 3),
+    lambda: pins.test_gelu_closed_form(),
+    lambda: pins.test_b2_added_once(),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+    mut = tmp_path / "oracle_mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-o", str(lib), str(mut), "-lm"], check=True)
+    caught = []
+    with oracle._library(str(lib)):
+        for call in PIN_CALLS:
+            try:
+                call()
+            except AssertionError:
+                caught.append(call)
+    assert caught, f"no pin caught the planted mistake: {name}"
