@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Throughput of the tensor-parallel MLP block (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = tpmlp_forward then tpmlp_backward (all six GEMMs and both bias
+gradients) over one batch of seeded synthetic input of the named workload
+(default: the 175B-class layer, T=2048 tokens, h=12288, f=49152, t=8).  The
+value is fwd+bwd TFLOP/s (12*T*h*f FLOP per step) over all ranks; tokens/s and
+the fraction of the dense bf16 peak ride along.  Prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded token sample of the same layer per step (same metric and unit).
+Under torchrun with N > 1 every rank runs an independent replica of the
+block (weak scaling; the block needs no data exchange between replicas).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300; % of BF16 dense peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt_175b")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, l2_note):
+    return {"workload": f"{w.name}: T={w.tokens} (mb {w.micro_batch} x seq {w.seq}), "
+                        f"h={w.hidden}, f={w.ffn}, t={w.t}, seq_chunks={w.seq_chunks}",
+            "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn, "t": w.t,
+            "seq_chunks": w.seq_chunks, "sigma_w": w.sigma_w, "seed": 0, "l2": l2_note}
+
+
+# ---- clocks -----------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_selector(torch, dev_index):
+    try:
+        props = torch.cuda.get_device_properties(dev_index)
+        uuid = str(getattr(props, "uuid", "") or "")
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index]
+    return str(dev_index)
+
+
+# ---- CPU oracle ----------------------------------------------------------------------------
+
+class OracleSample:
+    """The fp64 oracle on the first T_s tokens of the workload (same weights)."""
+
+    def __init__(self, w, inputs):
+        import numpy as np
+        import oracle
+        from tensor_transformer_mlp_gemm_gb300.inputs import column_shards, row_shards
+        self.oracle = oracle
+        self.cores = len(os.sched_getaffinity(0))
+        oracle.set_threads(self.cores)
+        self.w = w
+        # fp64 copies prepared once, outside any timing (input conversion only)
+        self.A = [np.ascontiguousarray(a.double().numpy()) for a in column_shards(inputs["A"], w.t)]
+        self.B = [np.ascontiguousarray(b.double().numpy()) for b in row_shards(inputs["B"], w.t)]
+        self.b1 = inputs["b1"].double().numpy()
+        self.b2 = inputs["b2"].double().numpy()
+        self.X = inputs["X"].double().numpy()
+        self.dZ = inputs["dZ"].double().numpy()
+
+    def run(self, tokens: int) -> float:
+        X = self.X[:tokens]
+        dZ = self.dZ[:tokens]
+        t0 = time.perf_counter()
+        self.oracle.forward_backward(X, self.A, self.b1, self.B, self.b2, dZ)
+        return time.perf_counter() - t0
+
+    def calibrate(self, target_s: float, start: int | None = None, cap: int | None = None) -> int:
+        tok = start or max(8, self.cores)
+        cap = cap or self.w.tokens
+        tok = min(tok, cap)
+        dt = self.run(tok)
+        if dt <= 0:
+            return tok
+        want = int(tok * target_s / dt)
+        want = max(self.cores, (want // self.cores) * self.cores) if want >= self.cores else max(1, want)
+        return max(1, min(cap, want))
+
+
+def cpu_baseline(w, inputs, target_s: float) -> dict:
+    smp = OracleSample(w, inputs)
+    tok = smp.calibrate(target_s)
+    dt = smp.run(tok)
+    flops = 12.0 * tok * w.hidden * w.ffn
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": smp.cores, "kind": "oracle",
+            "tokens_per_s": tok / dt, "seconds": dt,
+            "sample": f"fp64 oracle fwd+bwd on the first {tok} of {w.tokens} tokens of the same "
+                      f"layer (h={w.hidden}, f={w.ffn}, t={w.t}), same weights; "
+                      f"{flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
+
+
+# ---- distributed ----------------------------------------------------------------------------
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def barrier(dist, torch):
+    if dist is not None:
+        dist.barrier()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(dist, torch, x: float) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- arms -------------------------------------------------------------------------------------
+
+def run_reference(args, torch):
+    """The oracle arm: fp64 CPU oracle, rank 0 only, bounded token samples."""
+    from tensor_transformer_mlp_gemm_gb300.inputs import WORKLOADS, make_inputs
+    dist, rank, world, _ = dist_setup(torch)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    w = WORKLOADS[args.workload]
+    inputs = make_inputs(w, 0)
+    smp = OracleSample(w, inputs)
+    per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    tok = smp.calibrate(per_step, start=min(w.tokens, max(4, smp.cores // 2)))
+    for _ in range(args.warmup):
+        smp.run(tok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        smp.run(tok)
+    dt = time.perf_counter() - t0
+    flops = 12.0 * tok * w.hidden * w.ffn * args.steps
+    value = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, "host memory (CPU oracle)"),
+            "tokens_per_s": tok * args.steps / dt,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": smp.cores,
+                             "kind": "oracle",
+                             "sample": f"each step: fp64 oracle fwd+bwd on the first {tok} of "
+                                       f"{w.tokens} tokens of the layer, same weights"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_ours(args, torch):
+    from tensor_transformer_mlp_gemm_gb300.build import build
+    dist, rank, world, local = dist_setup(torch)
+    if rank == 0:
+        build()
+    if dist is not None:
+        dist.barrier()
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
+    from tensor_transformer_mlp_gemm_gb300.inputs import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inputs = make_inputs(w, 0)
+    blk = DeviceBlock(w, inputs, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    T, h, f = w.tokens, w.hidden, w.ffn
+    flops_step = 12.0 * T * h * f
+    weight_bytes = 2 * h * f * 2
+    l2_note = (f"inputs larger than L2 (bf16 weights {weight_bytes / 1e9:.2f} GB, "
+               f"activations {3 * T * f * 2 / 1e9:.2f} GB per step)")
+
+    # warm-up, then the timed device-resident loop
+    for _ in range(args.warmup):
+        blk.step(stream)
+    st = binding.tpmlp_sync_check(stream)
+    if st != binding.TPMLP_OK:
+        raise RuntimeError(f"warm-up failed: {binding.tpmlp_status_string(st)}")
+    barrier(dist, torch)
+    sampler = ClockSampler(gpu_selector(torch, local))
+    sampler.start()
+    time.sleep(0.5)
+    binding.tpmlp_profile_begin(16 * args.steps + 16)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist, torch)
+    e0.record(stream)
+    for _ in range(args.steps):
+        blk.step(stream)
+    e1.record(stream)
+    barrier(dist, torch)
+    kms, kcount = binding.tpmlp_profile_end()
+    clocks = sampler.stop()
+    st = binding.tpmlp_sync_check(stream)
+    if st != binding.TPMLP_OK:
+        raise RuntimeError(f"timed loop failed: {binding.tpmlp_status_string(st)}")
+    ms = max_over_ranks(dist, torch, e0.elapsed_time(e1))
+    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
+    tokens_s = T * args.steps * world / (ms / 1e3)
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel: the kernel kind with the largest share of device time
+    total_k = sum(kms.values())
+    kernels = {}
+    for name in kms:
+        if kcount[name]:
+            kernels[name] = {"launches": kcount[name], "ms_per_launch": kms[name] / kcount[name],
+                             "share": kms[name] / total_k if total_k else None}
+    gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
+    dom = max(kernels, key=lambda k: kms[k])
+    if dom in gemm_kinds:
+        achieved = 2.0 * T * h * f / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long "
+                               f"step); frac of burst {peaks['bf16_tflops']}: "
+                               f"{achieved / peaks['bf16_tflops']:.3f}",
+                "flops_per_launch": 2.0 * T * h * f}
+    else:
+        gb = (T * f * 2 + T * h * 2) / 1e9
+        achieved = gb / (kms[dom] / kcount[dom] / 1e3)
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    for name in gemm_kinds:
+        if name in kernels:
+            kernels[name]["tflops"] = 2.0 * T * h * f / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
+    launches_per_step = sum(kcount.values()) / args.steps
+
+    # end to end through the C ABI with host buffers: per step H2D of X and dZ
+    # from pinned memory, forward, D2H of Z, backward, D2H of dX
+    hX = [x.cpu().pin_memory() for x in blk.X]
+    hdZ = [x.cpu().pin_memory() for x in blk.dZ]
+    hZ = [torch.empty_like(z, device="cpu").pin_memory() for z in blk.Z]
+    hdX = [torch.empty_like(z, device="cpu").pin_memory() for z in blk.dX]
+
+    def e2e_step():
+        for d, s in zip(blk.X, hX):
+            d.copy_(s, non_blocking=True)
+        blk.forward(stream)
+        for d, s in zip(hZ, blk.Z):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(blk.dZ, hdZ):
+            d.copy_(s, non_blocking=True)
+        blk.backward(stream)
+        for d, s in zip(hdX, blk.dX):
+            d.copy_(s, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist, torch)
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    barrier(dist, torch)
+    st = binding.tpmlp_sync_check(stream)
+    if st != binding.TPMLP_OK:
+        raise RuntimeError(f"e2e loop failed: {binding.tpmlp_status_string(st)}")
+    ms_e2e = max_over_ranks(dist, torch, e2.elapsed_time(e3))
+    e2e = {"value": flops_step * args.e2e_steps * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": sum(x.numel() * 2 for x in hX + hdZ),
+           "d2h_bytes_per_step": sum(x.numel() * 2 for x in hZ + hdX),
+           "tokens_per_s": T * args.e2e_steps * world / (ms_e2e / 1e3),
+           "steps": args.e2e_steps}
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(w, inputs, args.cpu_seconds)
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(w, l2_note),
+                "tokens_per_s": tokens_s,
+                "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
+                                     "sustained": value / world / peaks["bf16_tflops_sustained"],
+                                     "source": peak_src},
+                "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks, "gpu_launches": int(sum(kcount.values())),
+                "gpu_launches_per_step": launches_per_step}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    import torch
+    if args.impl == "reference":
+        run_reference(args, torch)
+    else:
+        run_ours(args, torch)
+
+
+if __name__ == "__main__":
+    main()

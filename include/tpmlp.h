@@ -1,0 +1,189 @@
+/*
+ * tpmlp.h -- C ABI of libtpmlp: the tensor-parallel Transformer MLP block,
+ * forward and backward, on one sm_103 GPU.
+ *
+ *     Z = GeLU(X.A + b1).B + b2
+ *
+ * Sources (page title, section):
+ *   [FGO]    "Megatron-LM：NVIDIA 的大规模并行训练方案", section
+ *            "Megatron-LM 核心架构 / 张量并行原理": Y = XA; A split by
+ *            columns [A_1, A_2] gives Y_i = X.A_i (column parallel); A split
+ *            by rows with X split by columns gives Y = sum_i X_i.A_i summed by
+ *            an AllReduce (row parallel); the MLP's first linear is column
+ *            parallel and its second row parallel.
+ *   [FGO-F]  same page, "融合优化技术": Bias + GeLU fused into one kernel.
+ *   [FGO-SP] same page, "并行训练范式 / 序列并行": sequence parallelism on
+ *            top of tensor parallelism, along the sequence dimension.
+ *   [CH2]    "2、分布式训练基础：数据并行、模型并行、流水线并行的基本概念与区别",
+ *            "2.2 模型并行 —— 张量并行 / 核心原理": column-parallel split
+ *            [W1, W2], row-parallel split [W1; W2] with X = [X1, X2] and an
+ *            AllReduce sum.
+ *
+ * All t shards live on the one GPU; the row-parallel AllReduce of the
+ * forward pass (and its conjugate in the backward pass) becomes an on-chip
+ * split-K accumulation over the shards.  In the sequence-parallel variant X
+ * and dZ arrive as seq_chunks token chunks and Z and dX leave in the same
+ * chunking: the gather before the column-parallel GEMM is done by addressing
+ * the chunks directly, the reduce-scatter after the row-parallel GEMM by the
+ * split-K accumulation plus a row-to-chunk mapping in the GEMM's epilogue.
+ *
+ * Conventions for every call:
+ *   - All matrices are dense, row-major, with the shapes given below.
+ *     Notation: T = tokens, h = hidden, f = ffn, fi = f / t, Tc = T / seq_chunks.
+ *   - All buffer pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller, 16-byte aligned.  The library never allocates
+ *     or frees device memory during a forward/backward call.
+ *   - Pointer-array arguments ("const void* const*") are HOST arrays of
+ *     device pointers (one per shard or per chunk); the library copies the
+ *     pointers during the call and does not keep the host array.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  A returned TPMLP_OK means the
+ *     work was validated and enqueued; device-side failures (a bounded wait
+ *     that expired) are reported by tpmlp_sync_check().
+ *   - Validation failures return an error before anything is launched and
+ *     leave every output untouched.  Nothing crosses the ABI as an exception.
+ *   - Results are bitwise reproducible run to run (no atomics in any sum).
+ *   - Thread-compatible: concurrent calls from several host threads are
+ *     allowed on different streams with different workspaces.
+ *
+ * Requirements (else TPMLP_ERR_UNSUPPORTED): an sm_103 device; h and fi
+ * multiples of 8; 1 <= t <= 8; 1 <= seq_chunks <= 8 dividing T, and, when
+ * seq_chunks > 1, Tc a multiple of 128; T, h, f below 2^31.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TPMLP_OK = 0,
+    TPMLP_ERR_INVALID_ARG = 1,  /* null pointer, bad dims, t mismatch */
+    TPMLP_ERR_UNSUPPORTED = 2,  /* shape/alignment/device outside the requirements */
+    TPMLP_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    TPMLP_ERR_TIMEOUT = 4       /* a bounded device wait expired (see tpmlp_sync_check) */
+} tpmlp_status;
+
+typedef struct {
+    int64_t tokens;      /* T: micro-batch x sequence rows, sequence-major */
+    int64_t hidden;      /* h */
+    int64_t ffn;         /* f */
+    int32_t t;           /* tensor-parallel shards (1..8) */
+    int32_t seq_chunks;  /* 1, or the sequence-parallel degree (normally t) */
+} tpmlp_dims;
+
+/* Bytes of device workspace a forward/backward pair needs: the saved
+ * pre-activation Y and activation H (written by tpmlp_forward, read by
+ * tpmlp_backward), the gradient dY (written and read by tpmlp_backward) and
+ * the bias-gradient partial sums.  The caller allocates it (256-byte aligned
+ * is best) and keeps it alive from the forward to the matching backward. */
+size_t tpmlp_workspace_bytes(const tpmlp_dims* dims);
+
+/* Byte offsets inside the workspace of Y, H and dY, each stored shard-major
+ * as t blocks [T, fi] bf16 (shard i at offset + i*T*fi*2).  Any output may be
+ * NULL.  Lets a caller inspect the saved activations. */
+tpmlp_status tpmlp_workspace_layout(const tpmlp_dims* dims, size_t* y_offset,
+                                    size_t* h_offset, size_t* dy_offset);
+
+/* Forward pass ([FGO] 张量并行原理, [CH2] 2.2, [FGO-F] 融合优化技术):
+ *   for each shard i:  Y_i = X.A_i + b1[i*fi:(i+1)*fi],  H_i = GeLU(Y_i)
+ *   Z = (sum_i H_i.B_i) + b2          (b2 added once, after the shard sum)
+ * GeLU is the tanh form 0.5 y (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3))).
+ *   X        [seq_chunks] chunks of [Tc, h] bf16 (chunk j = token rows j*Tc..)
+ *   A_shards [t] shards of [h, fi] bf16   (column block i of A)
+ *   b1       [f] bf16
+ *   B_shards [t] shards of [fi, h] bf16   (row block i of B)
+ *   b2       [h] bf16
+ *   t        must equal dims->t
+ *   Z        [seq_chunks] chunks of [Tc, h] bf16 (output)
+ *   workspace  >= tpmlp_workspace_bytes(dims) bytes; Y and H are saved there
+ * Products accumulate in fp32 on the tensor cores; bias and GeLU are applied
+ * in fp32 in the GEMM epilogue; Y, H and Z are rounded to bf16 once. */
+tpmlp_status tpmlp_forward(const tpmlp_dims* dims,
+                           const void* const* X,
+                           const void* const* A_shards, const void* b1,
+                           const void* const* B_shards, const void* b2,
+                           int t,
+                           void* const* Z,
+                           void* workspace, void* stream);
+
+/* Backward pass: the chain rule of tpmlp_forward for upstream gradient dZ.
+ *   dY_i = (dZ.B_i^T) * GeLU'(Y_i)   (kept in the workspace, bf16)
+ *   dX   = sum_i dY_i.A_i^T          (the backward AllReduce, on chip)
+ *   dA_i = X^T.dY_i,  dB_i = H_i^T.dZ,
+ *   db1  = column sums of dY, db2 = column sums of dZ.
+ *   dZ        [seq_chunks] chunks of [Tc, h] bf16
+ *   X, A_shards, B_shards   as passed to tpmlp_forward
+ *   workspace the workspace of the matching tpmlp_forward (Y, H read; dY written)
+ *   dX        [seq_chunks] chunks of [Tc, h] bf16 (output)
+ *   dA_shards [t] of [h, fi] fp32 (output, overwritten)
+ *   db1       [f] fp32 (output, overwritten)
+ *   dB_shards [t] of [fi, h] fp32 (output, overwritten)
+ *   db2       [h] fp32 (output, overwritten)
+ * With T = 0 the weight and bias gradients are set to zero. */
+tpmlp_status tpmlp_backward(const tpmlp_dims* dims,
+                            const void* const* dZ,
+                            const void* const* X,
+                            const void* const* A_shards,
+                            const void* const* B_shards,
+                            void* workspace,
+                            void* const* dX,
+                            void* const* dA_shards, void* db1,
+                            void* const* dB_shards, void* db2,
+                            void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* tpmlp_status_string(tpmlp_status s);
+
+/* Synchronises the stream, then reports: TPMLP_ERR_CUDA if a CUDA error is
+ * pending, TPMLP_ERR_TIMEOUT if a kernel of this library gave up on a bounded
+ * wait since the last check (the device error word is then cleared), else
+ * TPMLP_OK.  Kernels that time out stop early, leave their outputs
+ * incomplete, release their tensor memory and return; the context stays
+ * usable. */
+tpmlp_status tpmlp_sync_check(void* stream);
+
+/* Upper bound, in nanoseconds, on any single wait inside a kernel of this
+ * library (default 2e9).  Affects launches enqueued after the call. */
+tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);
+
+/* Failure-detection self-test.  Runs one 128 x 256 x 64 GEMM tile whose
+ * loader deliberately issues no loads, so the tensor-core issuer's wait on
+ * its first stage can only end by the bounded-wait limit; the kernel then
+ * records the timeout, drains, frees its tensor memory and returns.
+ *   a  [128, 64] bf16 device buffer, b [256, 64] bf16, c [128, 256] bf16
+ *   (valid buffers of at least those sizes; c may be partially written).
+ * Synchronises the stream and returns what tpmlp_sync_check returns:
+ * TPMLP_ERR_TIMEOUT when the failure was detected as designed. */
+tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b, void* c,
+                                         uint64_t timeout_ns, void* stream);
+
+/* Kernel-level timing.  Between tpmlp_profile_begin and tpmlp_profile_end
+ * the library records a CUDA event pair on the launch stream around each of
+ * its kernel launches (at most `capacity` launches).  tpmlp_profile_end
+ * synchronises on those events and writes, for each kernel kind k <
+ * nkinds, the summed milliseconds ms[k] and the launch count launches[k];
+ * it returns the number of launches recorded, or -1 on error. */
+enum {
+    TPMLP_KERNEL_COLUMN_FWD = 0,  /* Y_i = X.A_i + b1, H_i = GeLU(Y_i) */
+    TPMLP_KERNEL_ROW_FWD = 1,     /* Z = sum_i H_i.B_i + b2 */
+    TPMLP_KERNEL_DGRAD_H = 2,     /* dY_i = (dZ.B_i^T) * GeLU'(Y_i) */
+    TPMLP_KERNEL_DGRAD_X = 3,     /* dX = sum_i dY_i.A_i^T */
+    TPMLP_KERNEL_WGRAD_B = 4,     /* dB_i = H_i^T.dZ */
+    TPMLP_KERNEL_WGRAD_A = 5,     /* dA_i = X^T.dY_i */
+    TPMLP_KERNEL_BIAS_GRAD = 6,   /* db1, db2 column sums (all launches) */
+    TPMLP_KERNEL_KINDS = 7
+};
+tpmlp_status tpmlp_profile_begin(int capacity);
+int tpmlp_profile_end(double* ms, int* launches, int nkinds);
+const char* tpmlp_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

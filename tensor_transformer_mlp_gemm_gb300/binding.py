@@ -1,0 +1,179 @@
+"""ctypes binding of libtpmlp (include/tpmlp.h), same names as the C ABI.
+
+Argument marshalling only: torch tensors become device pointers, lists become
+host pointer arrays, a non-OK status becomes a :class:`TpmlpError`.  Every step
+of the MLP block runs in the library's CUDA kernels.  There is no fallback: if
+the library has not been built, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libtpmlp.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"libtpmlp.so is not built ({_LIB_PATH}); run "
+        "`python -m tensor_transformer_mlp_gemm_gb300.build` (nvcc, sm_103a)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+TPMLP_OK = 0
+TPMLP_ERR_INVALID_ARG = 1
+TPMLP_ERR_UNSUPPORTED = 2
+TPMLP_ERR_CUDA = 3
+TPMLP_ERR_TIMEOUT = 4
+
+KERNEL_KINDS = 7
+
+# every symbol include/tpmlp.h declares
+EXPORTED = (
+    "tpmlp_workspace_bytes", "tpmlp_workspace_layout", "tpmlp_forward", "tpmlp_backward",
+    "tpmlp_status_string", "tpmlp_sync_check", "tpmlp_set_wait_timeout_ns",
+    "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
+    "tpmlp_kernel_name",
+)
+
+
+class tpmlp_dims(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("t", ctypes.c_int32), ("seq_chunks", ctypes.c_int32)]
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tpmlp_status_string(status)} (status {status})")
+
+
+_vp = ctypes.c_void_p
+_vpp = ctypes.POINTER(ctypes.c_void_p)
+_dims_p = ctypes.POINTER(tpmlp_dims)
+_sz_p = ctypes.POINTER(ctypes.c_size_t)
+
+_lib.tpmlp_workspace_bytes.restype = ctypes.c_size_t
+_lib.tpmlp_workspace_bytes.argtypes = [_dims_p]
+_lib.tpmlp_workspace_layout.restype = ctypes.c_int
+_lib.tpmlp_workspace_layout.argtypes = [_dims_p, _sz_p, _sz_p, _sz_p]
+_lib.tpmlp_forward.restype = ctypes.c_int
+_lib.tpmlp_forward.argtypes = [_dims_p, _vpp, _vpp, _vp, _vpp, _vp, ctypes.c_int, _vpp, _vp, _vp]
+_lib.tpmlp_backward.restype = ctypes.c_int
+_lib.tpmlp_backward.argtypes = [_dims_p, _vpp, _vpp, _vpp, _vpp, _vp, _vpp, _vpp, _vp, _vpp, _vp, _vp]
+_lib.tpmlp_status_string.restype = ctypes.c_char_p
+_lib.tpmlp_status_string.argtypes = [ctypes.c_int]
+_lib.tpmlp_sync_check.restype = ctypes.c_int
+_lib.tpmlp_sync_check.argtypes = [_vp]
+_lib.tpmlp_set_wait_timeout_ns.restype = ctypes.c_int
+_lib.tpmlp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+_lib.tpmlp_selftest_stalled_gemm.restype = ctypes.c_int
+_lib.tpmlp_selftest_stalled_gemm.argtypes = [_vp, _vp, _vp, ctypes.c_uint64, _vp]
+_lib.tpmlp_profile_begin.restype = ctypes.c_int
+_lib.tpmlp_profile_begin.argtypes = [ctypes.c_int]
+_lib.tpmlp_profile_end.restype = ctypes.c_int
+_lib.tpmlp_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
+                                   ctypes.c_int]
+_lib.tpmlp_kernel_name.restype = ctypes.c_char_p
+_lib.tpmlp_kernel_name.argtypes = [ctypes.c_int]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    return _lib
+
+
+def make_dims(tokens: int, hidden: int, ffn: int, t: int, seq_chunks: int = 1) -> tpmlp_dims:
+    return tpmlp_dims(int(tokens), int(hidden), int(ffn), int(t), int(seq_chunks))
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _arr(xs):
+    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != TPMLP_OK:
+        raise TpmlpError(status, where)
+
+
+def tpmlp_status_string(status: int) -> str:
+    return _lib.tpmlp_status_string(int(status)).decode()
+
+
+def tpmlp_kernel_name(kind: int) -> str:
+    return _lib.tpmlp_kernel_name(int(kind)).decode()
+
+
+def tpmlp_workspace_bytes(dims: tpmlp_dims) -> int:
+    return int(_lib.tpmlp_workspace_bytes(ctypes.byref(dims)))
+
+
+def tpmlp_workspace_layout(dims: tpmlp_dims) -> tuple[int, int, int]:
+    y, h, dy = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.tpmlp_workspace_layout(ctypes.byref(dims), ctypes.byref(y), ctypes.byref(h),
+                                       ctypes.byref(dy)), "tpmlp_workspace_layout")
+    return y.value, h.value, dy.value
+
+
+def tpmlp_forward(dims, X, A_shards, b1, B_shards, b2, t, Z, workspace, stream=None) -> None:
+    """X, Z: lists of seq_chunks tensors; A_shards, B_shards: lists of t tensors."""
+    _check(_lib.tpmlp_forward(ctypes.byref(dims), _arr(X), _arr(A_shards), _ptr(b1),
+                              _arr(B_shards), _ptr(b2), int(t), _arr(Z), _ptr(workspace),
+                              _stream(stream)), "tpmlp_forward")
+
+
+def tpmlp_backward(dims, dZ, X, A_shards, B_shards, workspace, dX, dA_shards, db1, dB_shards,
+                   db2, stream=None) -> None:
+    _check(_lib.tpmlp_backward(ctypes.byref(dims), _arr(dZ), _arr(X), _arr(A_shards),
+                               _arr(B_shards), _ptr(workspace), _arr(dX), _arr(dA_shards),
+                               _ptr(db1), _arr(dB_shards), _ptr(db2), _stream(stream)),
+           "tpmlp_backward")
+
+
+def tpmlp_sync_check(stream=None) -> int:
+    """Returns the status (does not raise), so callers can test for TIMEOUT."""
+    return int(_lib.tpmlp_sync_check(_stream(stream)))
+
+
+def tpmlp_set_wait_timeout_ns(ns: int) -> None:
+    _check(_lib.tpmlp_set_wait_timeout_ns(int(ns)), "tpmlp_set_wait_timeout_ns")
+
+
+def tpmlp_selftest_stalled_gemm(a, b, c, timeout_ns: int, stream=None) -> int:
+    return int(_lib.tpmlp_selftest_stalled_gemm(_ptr(a), _ptr(b), _ptr(c), int(timeout_ns),
+                                                _stream(stream)))
+
+
+def tpmlp_profile_begin(capacity: int) -> None:
+    _check(_lib.tpmlp_profile_begin(int(capacity)), "tpmlp_profile_begin")
+
+
+def tpmlp_profile_end() -> tuple[dict, dict]:
+    ms = (ctypes.c_double * KERNEL_KINDS)()
+    cnt = (ctypes.c_int * KERNEL_KINDS)()
+    n = _lib.tpmlp_profile_end(ms, cnt, KERNEL_KINDS)
+    if n < 0:
+        raise TpmlpError(TPMLP_ERR_CUDA, "tpmlp_profile_end")
+    names = [tpmlp_kernel_name(k) for k in range(KERNEL_KINDS)]
+    return ({names[k]: ms[k] for k in range(KERNEL_KINDS)},
+            {names[k]: cnt[k] for k in range(KERNEL_KINDS)})

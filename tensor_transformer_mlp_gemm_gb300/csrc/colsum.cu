@@ -1,0 +1,131 @@
+// colsum.cu -- HBM-bound column sums for the bias gradients db1 and db2.
+//
+// CTA = 256 threads over a 64-column strip: thread (slot, vec) reads the
+// 16-byte vector of 8 bf16 at columns vec*8.. of rows slot, slot+32, ...
+// (each warp covers four full 128-byte rows per load, coalesced), keeps 8
+// fp32 partial sums in registers, and the 32 row slots are then combined in
+// a fixed order through shared memory.  With row splits, a second kernel
+// adds the per-split partial sums in split order.  No atomics, so the result
+// is bitwise reproducible.
+#include <cuda_bf16.h>
+
+#include "colsum.cuh"
+
+namespace tpmlp {
+
+__device__ __forceinline__ void add_bf16x8(const uint4& u, float (&acc)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(CS_THREADS) colsum_kernel(const ColsumParams p) {
+    __shared__ float red[32][CS_COLS + 1];
+    const int vec = threadIdx.x & 7;
+    const int slot = threadIdx.x >> 3;
+    const int grp = blockIdx.z;
+    const int col = blockIdx.x * CS_COLS + vec * 8;
+    const long long total_rows =
+        p.mode == CS_ROWS_CONCAT ? p.rows_per_part * p.nparts : p.rows_per_part;
+    const long long r0 = static_cast<long long>(blockIdx.y) * p.rows_per_split;
+    const long long r1 = min(total_rows, r0 + p.rows_per_split);
+
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+
+    if (col < p.ncols) {
+        long long r = r0 + slot;
+        // four independent loads in flight per thread
+        for (; r + 96 < r1; r += 128) {
+            uint4 u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const long long rr = r + 32 * q;
+                int part = grp;
+                long long lr = rr;
+                if (p.mode == CS_ROWS_CONCAT) {
+                    part = static_cast<int>(rr / p.rows_per_part);
+                    lr = rr - part * p.rows_per_part;
+                }
+                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.src[part]);
+                u[q] = __ldg(reinterpret_cast<const uint4*>(src + lr * p.ncols + col));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) add_bf16x8(u[q], acc);
+        }
+        for (; r < r1; r += 32) {
+            int part = grp;
+            long long lr = r;
+            if (p.mode == CS_ROWS_CONCAT) {
+                part = static_cast<int>(r / p.rows_per_part);
+                lr = r - part * p.rows_per_part;
+            }
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.src[part]);
+            add_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + lr * p.ncols + col)), acc);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) red[slot][vec * 8 + j] = acc[j];
+    __syncthreads();
+    if (threadIdx.x < CS_COLS) {
+        const int c = blockIdx.x * CS_COLS + threadIdx.x;
+        if (c < p.ncols) {
+            float s = 0.f;
+            for (int k = 0; k < 32; ++k) s += red[k][threadIdx.x];
+            const long long n_out =
+                p.mode == CS_ROWS_CONCAT ? p.ncols : static_cast<long long>(p.ncols) * p.nparts;
+            const long long o = (p.mode == CS_COLS_CONCAT ? static_cast<long long>(grp) * p.ncols : 0) + c;
+            if (p.splits == 1)
+                p.out[o] = s;
+            else
+                p.partial[static_cast<long long>(blockIdx.y) * n_out + o] = s;
+        }
+    }
+}
+
+__global__ void colsum_finish_kernel(const float* __restrict__ partial, int splits,
+                                     long long n_out, float* __restrict__ out) {
+    const long long o = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (o >= n_out) return;
+    float s = 0.f;
+    for (int k = 0; k < splits; ++k) s += partial[k * n_out + o];
+    out[o] = s;
+}
+
+dim3 colsum_plan(ColsumParams& p, int sm_count) {
+    const int strips = (p.ncols + CS_COLS - 1) / CS_COLS;
+    const int groups = p.mode == CS_COLS_CONCAT ? p.nparts : 1;
+    const long long total_rows =
+        p.mode == CS_ROWS_CONCAT ? p.rows_per_part * p.nparts : p.rows_per_part;
+    const long long base = static_cast<long long>(strips) * groups;
+    long long splits = (4LL * sm_count + base - 1) / base;
+    const long long max_by_rows = total_rows / 256 > 0 ? total_rows / 256 : 1;
+    if (splits > max_by_rows) splits = max_by_rows;
+    if (splits > CS_MAX_SPLITS) splits = CS_MAX_SPLITS;
+    if (splits < 1) splits = 1;
+    p.splits = static_cast<int>(splits);
+    p.rows_per_split = (total_rows + splits - 1) / splits;
+    if (p.rows_per_split < 1) p.rows_per_split = 1;
+    return dim3(strips, p.splits, groups);
+}
+
+cudaError_t launch_colsum(const ColsumParams& p, dim3 grid, cudaStream_t stream, int* launches) {
+    colsum_kernel<<<grid, CS_THREADS, 0, stream>>>(p);
+    int n = 1;
+    if (p.splits > 1) {
+        const long long n_out =
+            p.mode == CS_ROWS_CONCAT ? p.ncols : static_cast<long long>(p.ncols) * p.nparts;
+        const int threads = 256;
+        const unsigned blocks = static_cast<unsigned>((n_out + threads - 1) / threads);
+        colsum_finish_kernel<<<blocks, threads, 0, stream>>>(p.partial, p.splits, n_out, p.out);
+        ++n;
+    }
+    if (launches) *launches = n;
+    return cudaGetLastError();
+}
+
+}  // namespace tpmlp

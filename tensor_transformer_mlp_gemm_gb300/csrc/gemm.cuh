@@ -1,0 +1,439 @@
+// gemm.cuh -- the tcgen05 GEMM behind every contraction of the tensor-parallel
+// MLP block, with the block's elementwise work fused into its epilogue.
+//
+// Sources (page title, section):
+//   [FGO]   "Megatron-LM：NVIDIA 的大规模并行训练方案", "Megatron-LM 核心架构 /
+//           张量并行原理" (column- and row-parallel linear layers, MLP = column
+//           then row).
+//   [FGO-F] same page, "融合优化技术" (Bias + GeLU fused into one kernel).
+//   [CH2]   "2、分布式训练基础：数据并行、模型并行、流水线并行的基本概念与区别",
+//           "2.2 模型并行 —— 张量并行 / 核心原理".
+//
+// One kernel computes, for every group g and output tile,
+//     C_g[m, n] = sum_{s < ksegs} sum_{k < K} Aop_{g,s}[m, k] * Bop_{g,s}[n, k]
+// where the operands are bf16 matrices reached through TMA tensor maps and the
+// sum runs in fp32 in tensor memory.  "Groups" are independent GEMMs that
+// share a launch (the t column-parallel shards); "k-segments" are summed into
+// the same accumulator (the t row-parallel shards: the AllReduce of the pages
+// becomes split-K accumulation in TMEM, with no separate reduction pass).
+//
+// Each operand is either K-major (row-major [rows, K]) or MN-major (row-major
+// [K, rows]); the weight-gradient GEMMs contract over tokens and read both
+// operands MN-major straight from the token-major activations.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer (one elected thread): A and B tiles into a
+//               STAGES-deep shared-memory ring, completion on mbarriers
+//   warp 1      owns the tensor memory; one elected thread issues
+//               tcgen05.mma (128 x 256 x 16 per instruction) and commits
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused elementwise
+//               work, bf16/fp32 stores
+// Two 256-column fp32 accumulators in TMEM let the epilogue of one tile run
+// under the main loop of the next.
+//
+// Every wait is bounded (GemmParams::timeout_ns).  A wait that expires sets a
+// CTA-wide abort flag and a bit of the device error word; every role then
+// leaves its loop, the producer waits (bounded) for its own copies in flight,
+// the MMA issuer waits (bounded) for its own MMAs, and the CTA frees its
+// tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace tpmlp {
+
+// ---- tanh-form GeLU ----------------------------------------------------------
+// GeLU(y)  = 0.5 y (1 + tanh(u)),  u = sqrt(2/pi) (y + 0.044715 y^3)
+// GeLU'(y) = 0.5 (1 + tanh u) + 0.5 y (1 - tanh^2 u) sqrt(2/pi) (1 + 3*0.044715 y^2)
+constexpr float kGeluK0 = 0.7978845608028654f;  // sqrt(2/pi)
+constexpr float kGeluK1 = 0.044715f;
+
+__device__ __forceinline__ float gelu_f(float y) {
+    const float u = kGeluK0 * fmaf(kGeluK1 * y, y * y, y);
+    return 0.5f * y * (1.0f + ptx::tanh_approx(u));
+}
+
+__device__ __forceinline__ float gelu_grad_f(float y) {
+    const float y2 = y * y;
+    const float u = kGeluK0 * fmaf(kGeluK1 * y, y2, y);
+    const float th = ptx::tanh_approx(u);
+    const float du = kGeluK0 * fmaf(3.0f * kGeluK1, y2, 1.0f);
+    return 0.5f * (1.0f + th) + 0.5f * y * (1.0f - th * th) * du;
+}
+
+// ---- bounded waits -------------------------------------------------------------
+
+// Waits for phase `parity` of `bar`.  Gives up (returns false) when another
+// role has aborted, or when timeout_ns has elapsed (then this role aborts the
+// CTA and records `code` in the device error word).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, const GemmParams& p,
+                                             unsigned code) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(p.err, code);
+            return false;
+        }
+    }
+}
+
+// Teardown wait: ignores the abort flag, still bounded.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.err, ERR_DRAIN);
+            return false;
+        }
+    }
+    return true;
+}
+
+// ---- tile schedule ---------------------------------------------------------------
+// Tiles are walked in bands of `band` M-tiles; inside a band the M-tile index
+// runs fastest, so the CTAs that run at the same time share their B tiles
+// (and, across the band, their A panels) through L2.  (group, n-tile) pairs
+// form one combined N axis.
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& g, int& m0,
+                                            int& n0) {
+    const int nt_total = p.ntiles * p.groups;
+    const int band_tiles = p.band * nt_total;
+    const int b = tile / band_tiles;
+    const int r = tile - b * band_tiles;
+    const int mt_first = b * p.band;
+    const int rows_here = min(p.band, p.mtiles - mt_first);
+    const int mt = mt_first + r % rows_here;
+    const int ntg = r / rows_here;
+    g = ntg / p.ntiles;
+    n0 = (ntg - g * p.ntiles) * BN;
+    m0 = mt * BM;
+}
+
+// ---- operand loads -----------------------------------------------------------------
+// K-major operand: tensor [rows, K] (inner K), box {BK, ROWS}; one copy.
+// MN-major operand: tensor [K, rows] (inner rows), box {64, BK}; ROWS/64
+// copies, box j landing at dst + j * MN_CHUNK_BYTES.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, int rows_per_map,
+                                             int g, int s, int row0, int kc, int K, uint32_t dst,
+                                             uint32_t bar) {
+    int idx = 0, r = row0, k = s * K + kc;
+    if (part == PART_GROUP) {
+        idx = g;
+    } else if (part == PART_KSEG) {
+        idx = s;
+        k = kc;
+    } else if (part == PART_ROW) {
+        idx = row0 / rows_per_map;
+        r = row0 - idx * rows_per_map;
+    }
+    const CUtensorMap* m = maps + idx;
+    if constexpr (!MN) {
+        ptx::tma_load_2d(dst, m, k, r, bar);
+    } else {
+#pragma unroll
+        for (int j = 0; j < ROWS / MN_CHUNK; ++j)
+            ptx::tma_load_2d(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
+    }
+}
+
+// Descriptor of the 16-wide K slice `kk` (0..3) of a stage's operand tile.
+//   K-major:  rows of 128 B, 8-row swizzle atoms stacked every 1024 B (SBO);
+//             the K slice starts 32 B further along the row.
+//   MN-major: [rows/64 boxes][BK K-rows][64 elements]; 8-K-row atoms every
+//             1024 B (SBO), 64-element boxes every MN_CHUNK_BYTES (LBO); the
+//             K slice starts 16 rows (2048 B) further down.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk) {
+    if constexpr (!MN)
+        return ptx::smem_desc_sw128(tile + kk * 32, 16, 1024);
+    else
+        return ptx::smem_desc_sw128(tile + kk * 2048, MN_CHUNK_BYTES, 1024);
+}
+
+// ---- epilogue ----------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// One thread: row m, columns [n, n+32) of the tile, accumulator values v.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int g, int m, int n,
+                                               const uint32_t (&v)[32]) {
+    if (m >= p.M) return;
+    int part = g;
+    long long row = m;
+    if (p.out_part == PART_ROW) {
+        part = m / p.out_rows_per_part;
+        row = m - static_cast<long long>(part) * p.out_rows_per_part;
+    }
+    const long long off = row * p.ld_out + n;
+
+    if constexpr (EPI == EPI_F32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out0[part]) + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (n + 4 * q < p.N)
+                o[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+    } else {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+
+        if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS) {
+            const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(p.bias) + n +
+                                     (EPI == EPI_BIAS_GELU ? g * p.bias_group_stride : 0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (n + 8 * q < p.N) {
+                    float bf[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(b + 8 * q), bf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] += bf[j];
+                }
+            }
+        }
+        if constexpr (EPI == EPI_DGELU) {
+            const __nv_bfloat16* y = static_cast<const __nv_bfloat16*>(p.in0[part]) + off;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (n + 8 * q < p.N) {
+                    float yf[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(y + 8 * q), yf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] *= gelu_grad_f(yf[j]);
+                }
+            }
+        }
+        uint4* o0 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0[part]) + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (n + 8 * q < p.N) {
+                const float* a = x + 8 * q;
+                o0[q] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                   pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+            }
+        }
+        if constexpr (EPI == EPI_BIAS_GELU) {
+            uint4* o1 =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out1[part]) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (n + 8 * q < p.N) {
+                    const float* a = x + 8 * q;
+                    o1[q] = make_uint4(pack_bf16x2(gelu_f(a[0]), gelu_f(a[1])),
+                                       pack_bf16x2(gelu_f(a[2]), gelu_f(a[3])),
+                                       pack_bf16x2(gelu_f(a[4]), gelu_f(a[5])),
+                                       pack_bf16x2(gelu_f(a[6]), gelu_f(a[7])));
+                }
+            }
+        }
+    }
+}
+
+// ---- the kernel ---------------------------------------------------------------------
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* bar_area = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    const uint32_t bar_full = bar0;                      // [STAGES]
+    const uint32_t bar_empty = bar0 + 8 * STAGES;        // [STAGES]
+    const uint32_t bar_tfull = bar0 + 16 * STAGES;       // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;          // [2]
+    const uint32_t bar_drain = bar_tempty + 16;          // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 16 * STAGES + 40);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 44);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(bar_tfull + 8 * a, 1);
+            ptx::mbar_init(bar_tempty + 8 * a, 4 * 32);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int kblocks = (p.K + BK - 1) / BK;
+    const int nk = kblocks * p.ksegs;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int stage = 0;
+            uint32_t phase = 0;
+            long long fills = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+                int g, m0, n0;
+                decode_tile(p, tile, g, m0, n0);
+                for (int s = 0; ok && s < p.ksegs; ++s) {
+                    for (int kb = 0; kb < kblocks; ++kb) {
+                        if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
+                                          ERR_PRODUCER)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!p.stall_producer) {
+                            const uint32_t full = bar_full + 8 * stage;
+                            const uint32_t sa = base + stage * STAGE_BYTES;
+                            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
+                            load_operand<A_MN, BM>(p.a_map, p.a_part, p.a_rows_per_map, g, s, m0,
+                                                   kb * BK, p.K, sa, full);
+                            load_operand<B_MN, BN>(p.b_map, p.b_part, p.b_rows_per_map, g, s, n0,
+                                                   kb * BK, p.K, sa + A_STAGE_BYTES, full);
+                            ++fills;
+                        }
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // Wait for this CTA's own copies still in flight (the last
+                // STAGES fills) before the CTA can leave.
+                for (long long f = (fills > STAGES ? fills - STAGES : 0); f < fills; ++f) {
+                    const int st = static_cast<int>(f % STAGES);
+                    const uint32_t par = static_cast<uint32_t>((f / STAGES) & 1);
+                    if (!wait_drain(bar_full + 8 * st, par, p)) break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int lt = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++lt) {
+                const int acc = lt & 1;
+                const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
+                if (!wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p, ERR_MMA)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p, ERR_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        ptx::mma_bf16_ss(d_tmem, operand_desc<A_MN>(sa, k),
+                                         operand_desc<B_MN>(sb, k), IDESC,
+                                         (kk > 0 || k > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar_empty + 8 * stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) ptx::mma_commit(bar_tfull + 8 * acc);
+            }
+            // Every MMA this thread issued must finish before TMEM is freed.
+            ptx::mma_commit(bar_drain);
+            wait_drain(bar_drain, 0, p);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++lt) {
+            int g, m0, n0;
+            decode_tile(p, tile, g, m0, n0);
+            const int acc = lt & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
+            const bool ok = wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag, p,
+                                         ERR_EPILOGUE);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            __syncwarp();
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+                ptx::tmem_ld_wait();
+                if (n0 + c * 32 < p.N) epilogue_chunk<EPI>(p, g, m0 + row, n0 + c * 32, v);
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_tempty + 8 * acc);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+#define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)                                           \
+    cudaError_t NAME(const GemmParams& p, int grid, cudaStream_t stream) {                      \
+        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;                                          \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                             GEMM_SMEM_BYTES);                                   \
+        if (e != cudaSuccess) return e;                                                          \
+        kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(p);                                \
+        return cudaGetLastError();                                                               \
+    }
+
+}  // namespace tpmlp

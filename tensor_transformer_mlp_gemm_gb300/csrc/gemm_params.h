@@ -1,0 +1,81 @@
+// gemm_params.h -- host-visible description of one launch of the tcgen05
+// GEMM (tile sizes, operand partitioning, epilogue kind) and the launchers
+// of its variants.  Shared by the C-ABI translation unit and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tpmlp {
+
+constexpr int BM = 128;       // tile rows (TMEM lanes)
+constexpr int BN = 256;       // tile columns (TMEM columns per accumulator)
+constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int GEMM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int MAX_MAPS = 8;
+constexpr int MN_CHUNK = 64;                      // elements per 128-byte row
+constexpr int MN_CHUNK_BYTES = MN_CHUNK * BK * 2;  // one MN-major box [BK][64]
+
+// How the tensor maps of an operand (or the output pointers) are indexed.
+enum Part : int {
+    PART_SINGLE = 0,  // one map; K coordinate runs over all segments
+    PART_GROUP = 1,   // map g; K coordinate runs over all segments
+    PART_KSEG = 2,    // map s; K coordinate within the segment
+    PART_ROW = 3      // map row0 / rows_per_map (token chunks); K over all segments
+};
+
+enum Epi : int {
+    EPI_BIAS_GELU = 1,  // out0 = bf16(acc + bias), out1 = bf16(GeLU(acc + bias))
+    EPI_BIAS = 2,       // out0 = bf16(acc + bias)
+    EPI_DGELU = 3,      // out0 = bf16(acc * GeLU'(in0))
+    EPI_BF16 = 4,       // out0 = bf16(acc)
+    EPI_F32 = 5         // out0 = acc (fp32)
+};
+
+// Error-word bits (which role gave up).
+constexpr unsigned ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_EPILOGUE = 4u, ERR_DRAIN = 8u;
+
+struct GemmParams {
+    CUtensorMap a_map[MAX_MAPS];
+    CUtensorMap b_map[MAX_MAPS];
+    int M, N, K;            // per-group output rows/cols; K per segment
+    int groups, ksegs;
+    int a_part, b_part;
+    int a_rows_per_map, b_rows_per_map;
+    int mtiles, ntiles, total_tiles, band;
+    // epilogue
+    void* out0[MAX_MAPS];
+    void* out1[MAX_MAPS];
+    const void* in0[MAX_MAPS];
+    const void* bias;
+    long long ld_out;        // leading dimension of out0/out1/in0 (elements)
+    int out_part;            // PART_GROUP or PART_ROW
+    int out_rows_per_part;   // rows per output chunk for PART_ROW
+    int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU)
+    // control
+    unsigned int* err;
+    unsigned long long timeout_ns;
+    int stall_producer;      // failure-detection self-test: issue no loads
+};
+
+// Launchers, one per (operand majorness, epilogue) variant.
+//   column_fwd : A K-major,  B MN-major, EPI_BIAS_GELU  (Y_i, H_i)
+//   row_fwd    : A K-major,  B MN-major, EPI_BIAS       (Z)
+//   dgrad_h    : A K-major,  B K-major,  EPI_DGELU      (dY_i)
+//   dgrad_x    : A K-major,  B K-major,  EPI_BF16       (dX)
+//   wgrad      : A MN-major, B MN-major, EPI_F32        (dA_i, dB_i)
+cudaError_t launch_column_fwd(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_row_fwd(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_dgrad_h(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_dgrad_x(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_wgrad(const GemmParams& p, int grid, cudaStream_t stream);
+
+}  // namespace tpmlp

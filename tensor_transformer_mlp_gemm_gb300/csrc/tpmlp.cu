@@ -1,0 +1,628 @@
+// tpmlp.cu -- the C ABI of libtpmlp (declared in include/tpmlp.h).
+//
+// Validates arguments, encodes the TMA tensor maps of every operand, lays out
+// the workspace, and enqueues the kernels of the forward and backward passes
+// of the tensor-parallel MLP block on the caller's stream:
+//
+//   forward   column_fwd  Y_i = X.A_i + b1_i, H_i = GeLU(Y_i)     (t groups)
+//             row_fwd     Z = sum_i H_i.B_i + b2                  (t k-segments)
+//   backward  dgrad_h     dY_i = (dZ.B_i^T) * GeLU'(Y_i)          (t groups)
+//             dgrad_x     dX = sum_i dY_i.A_i^T                   (t k-segments)
+//             wgrad       dB_i = H_i^T.dZ                         (t groups)
+//             wgrad       dA_i = X^T.dY_i                         (t groups)
+//             colsum      db1 = sum_T dY, db2 = sum_T dZ
+//
+// Sources (page title, section): "Megatron-LM：NVIDIA 的大规模并行训练方案",
+// "Megatron-LM 核心架构 / 张量并行原理" (column then row parallel MLP),
+// "融合优化技术" (Bias + GeLU fusion), "并行训练范式 / 序列并行" (sequence
+// parallelism); "2、分布式训练基础：数据并行、模型并行、流水线并行的基本概念与区别",
+// "2.2 模型并行 —— 张量并行 / 核心原理".
+//
+// Sequence parallelism: X and dZ come as seq_chunks token chunks, addressed
+// through one tensor map per chunk (the gather happens inside the TMA loads),
+// and the epilogues of the split-K GEMMs write each output row into its chunk
+// (the reduce-scatter); no staging copies.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/tpmlp.h"
+#include "colsum.cuh"
+#include "gemm_params.h"
+
+#define TPMLP_API extern "C" __attribute__((visibility("default")))
+
+namespace tpmlp {
+
+// Device error word: kernels OR a bit in when a bounded wait expires.
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxShards = 8;
+constexpr int kBand = 16;  // M-tiles per raster band
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+unsigned long long g_timeout_ns = 2000000000ULL;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// ---- profiling ------------------------------------------------------------------
+struct ProfRec {
+    int kind;
+    int kernels;  // kernel launches between the two events
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_pool;
+size_t g_prof_used = 0;
+
+ProfRec* prof_next(int kind, int kernels) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on || g_prof_used >= g_prof_pool.size()) return nullptr;
+    ProfRec* r = &g_prof_pool[g_prof_used++];
+    r->kind = kind;
+    r->kernels = kernels;
+    return r;
+}
+
+template <typename F>
+cudaError_t timed(int kind, int kernels, cudaStream_t s, F&& launch) {
+    ProfRec* r = prof_next(kind, kernels);
+    if (r) cudaEventRecord(r->a, s);
+    cudaError_t e = launch();
+    if (r) cudaEventRecord(r->b, s);
+    return e;
+}
+
+// ---- device / driver ----------------------------------------------------------------
+tpmlp_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TPMLP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TPMLP_ERR_CUDA;
+        d.supported = (prop.major == 10 && prop.minor == 3);
+        d.sm_count = prop.multiProcessorCount;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return TPMLP_ERR_CUDA;
+            d.err = static_cast<unsigned int*>(p);
+            if (cudaMemset(d.err, 0, sizeof(unsigned int)) != cudaSuccess) return TPMLP_ERR_CUDA;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return TPMLP_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return TPMLP_ERR_UNSUPPORTED;
+    *out = &d;
+    return TPMLP_OK;
+}
+
+// ---- tensor maps -------------------------------------------------------------------------
+// bf16 row-major matrix [outer, inner] with leading dimension ld (elements).
+//   K-major operand tile: box {BK, box_rows} (BK along the contiguous K axis)
+//   MN-major operand tile: box {64, BK}      (64 along the contiguous M/N axis)
+bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+                 uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, int box_rows) {
+    return encode_bf16(m, ptr, K, rows, K, BK, static_cast<uint32_t>(box_rows));
+}
+
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K) {
+    return encode_bf16(m, ptr, rows, K, rows, MN_CHUNK, BK);
+}
+
+// ---- workspace ---------------------------------------------------------------------------
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+    size_t y, h, dy, part1, part2, total;
+};
+
+Layout layout_of(const tpmlp_dims& d) {
+    Layout L;
+    const size_t act = align256(static_cast<size_t>(d.tokens) * static_cast<size_t>(d.ffn) * 2);
+    L.y = 0;
+    L.h = act;
+    L.dy = 2 * act;
+    L.part1 = 3 * act;
+    L.part2 = L.part1 + align256(colsum_scratch_bytes(d.ffn));
+    L.total = L.part2 + align256(colsum_scratch_bytes(d.hidden));
+    return L;
+}
+
+// ---- validation --------------------------------------------------------------------------
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tpmlp_status check_dims(const tpmlp_dims* d) {
+    if (!d) return TPMLP_ERR_INVALID_ARG;
+    if (d->tokens < 0 || d->hidden <= 0 || d->ffn <= 0 || d->t <= 0 || d->seq_chunks <= 0)
+        return TPMLP_ERR_INVALID_ARG;
+    if (d->ffn % d->t != 0) return TPMLP_ERR_INVALID_ARG;
+    if (d->tokens % d->seq_chunks != 0) return TPMLP_ERR_INVALID_ARG;
+    if (d->t > kMaxShards || d->seq_chunks > kMaxShards) return TPMLP_ERR_UNSUPPORTED;
+    const int64_t fi = d->ffn / d->t;
+    if (d->hidden % 8 != 0 || fi % 8 != 0) return TPMLP_ERR_UNSUPPORTED;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (d->tokens > lim || d->hidden > lim || d->ffn > lim) return TPMLP_ERR_UNSUPPORTED;
+    if (d->seq_chunks > 1 && (d->tokens / d->seq_chunks) % BM != 0) return TPMLP_ERR_UNSUPPORTED;
+    return TPMLP_OK;
+}
+
+tpmlp_status check_ptrs(const void* const* arr, int n) {
+    if (!arr) return TPMLP_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (!arr[i]) return TPMLP_ERR_INVALID_ARG;
+        if (!aligned16(arr[i])) return TPMLP_ERR_UNSUPPORTED;
+    }
+    return TPMLP_OK;
+}
+
+tpmlp_status check_ptr(const void* p) {
+    if (!p) return TPMLP_ERR_INVALID_ARG;
+    return aligned16(p) ? TPMLP_OK : TPMLP_ERR_UNSUPPORTED;
+}
+
+#define TPMLP_TRY(expr)                        \
+    do {                                       \
+        tpmlp_status _s = (expr);              \
+        if (_s != TPMLP_OK) return _s;         \
+    } while (0)
+
+#define TPMLP_CUDA(expr)                                \
+    do {                                                \
+        if ((expr) != cudaSuccess) return TPMLP_ERR_CUDA; \
+    } while (0)
+
+// ---- GEMM set-up ------------------------------------------------------------------------
+void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int groups,
+                 int ksegs) {
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.groups = groups;
+    p.ksegs = ksegs;
+    p.mtiles = (M + BM - 1) / BM;
+    p.ntiles = (N + BN - 1) / BN;
+    p.total_tiles = p.mtiles * p.ntiles * groups;
+    p.band = p.mtiles < kBand ? p.mtiles : kBand;
+    p.err = dev.err;
+    p.timeout_ns = g_timeout_ns;
+    p.stall_producer = 0;
+    p.bias = nullptr;
+    p.bias_group_stride = 0;
+    for (int i = 0; i < MAX_MAPS; ++i) {
+        p.out0[i] = nullptr;
+        p.out1[i] = nullptr;
+        p.in0[i] = nullptr;
+    }
+}
+
+int grid_for(const GemmParams& p, const DeviceInfo& dev) {
+    return p.total_tiles < dev.sm_count ? p.total_tiles : dev.sm_count;
+}
+
+struct Shapes {
+    int T, h, f, t, fi, chunks, Tc;
+};
+
+Shapes shapes_of(const tpmlp_dims& d) {
+    Shapes s;
+    s.T = static_cast<int>(d.tokens);
+    s.h = static_cast<int>(d.hidden);
+    s.f = static_cast<int>(d.ffn);
+    s.t = d.t;
+    s.fi = s.f / s.t;
+    s.chunks = d.seq_chunks;
+    s.Tc = s.T / s.chunks;
+    return s;
+}
+
+inline const void* shard_ptr(const void* base, int i, const Shapes& s) {
+    return static_cast<const uint8_t*>(base) + static_cast<size_t>(i) * s.T * s.fi * 2;
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+// =========================================================================================
+TPMLP_API const char* tpmlp_status_string(tpmlp_status s) {
+    switch (s) {
+        case TPMLP_OK: return "ok";
+        case TPMLP_ERR_INVALID_ARG: return "invalid argument";
+        case TPMLP_ERR_UNSUPPORTED: return "unsupported shape, alignment or device";
+        case TPMLP_ERR_CUDA: return "CUDA error";
+        case TPMLP_ERR_TIMEOUT: return "bounded device wait expired";
+    }
+    return "unknown status";
+}
+
+TPMLP_API size_t tpmlp_workspace_bytes(const tpmlp_dims* dims) {
+    if (check_dims(dims) != TPMLP_OK) return 0;
+    return layout_of(*dims).total;
+}
+
+TPMLP_API tpmlp_status tpmlp_workspace_layout(const tpmlp_dims* dims, size_t* y_offset,
+                                              size_t* h_offset, size_t* dy_offset) {
+    TPMLP_TRY(check_dims(dims));
+    const Layout L = layout_of(*dims);
+    if (y_offset) *y_offset = L.y;
+    if (h_offset) *h_offset = L.h;
+    if (dy_offset) *dy_offset = L.dy;
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns) {
+    if (ns == 0) return TPMLP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_timeout_ns = ns;
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* X,
+                                     const void* const* A_shards, const void* b1,
+                                     const void* const* B_shards, const void* b2, int t,
+                                     void* const* Z, void* workspace, void* stream) {
+    TPMLP_TRY(check_dims(dims));
+    if (t != dims->t) return TPMLP_ERR_INVALID_ARG;
+    const Shapes s = shapes_of(*dims);
+    TPMLP_TRY(check_ptrs(A_shards, s.t));
+    TPMLP_TRY(check_ptrs(B_shards, s.t));
+    TPMLP_TRY(check_ptr(b1));
+    TPMLP_TRY(check_ptr(b2));
+    if (s.T > 0) {
+        TPMLP_TRY(check_ptrs(X, s.chunks));
+        TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(Z), s.chunks));
+        TPMLP_TRY(check_ptr(workspace));
+    }
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    if (s.T == 0) return TPMLP_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Layout L = layout_of(*dims);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const void* Y = ws + L.y;
+    const void* H = ws + L.h;
+
+    // column-parallel GEMM + bias + GeLU: t groups, M = T, N = fi, K = h
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_kmajor(&p.a_map[j], X[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_ROW;
+        p.a_rows_per_map = s.Tc;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) {
+            p.out0[i] = const_cast<void*>(shard_ptr(Y, i, s));
+            p.out1[i] = const_cast<void*>(shard_ptr(H, i, s));
+        }
+        p.ld_out = s.fi;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        p.bias = b1;
+        p.bias_group_stride = s.fi;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_COLUMN_FWD, 1, st,
+                         [&] { return launch_column_fwd(p, grid_for(p, *dev), st); }));
+    }
+    // row-parallel GEMM, shard split-K + b2: M = T, N = h, K = fi per segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_kmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, BM))
+                return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi)) return TPMLP_ERR_UNSUPPORTED;
+        }
+        p.a_part = PART_KSEG;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int j = 0; j < s.chunks; ++j) p.out0[j] = Z[j];
+        p.ld_out = s.h;
+        p.out_part = PART_ROW;
+        p.out_rows_per_part = s.Tc;
+        p.bias = b2;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
+                         [&] { return launch_row_fwd(p, grid_for(p, *dev), st); }));
+    }
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const* dZ,
+                                      const void* const* X, const void* const* A_shards,
+                                      const void* const* B_shards, void* workspace,
+                                      void* const* dX, void* const* dA_shards, void* db1,
+                                      void* const* dB_shards, void* db2, void* stream) {
+    TPMLP_TRY(check_dims(dims));
+    const Shapes s = shapes_of(*dims);
+    TPMLP_TRY(check_ptrs(A_shards, s.t));
+    TPMLP_TRY(check_ptrs(B_shards, s.t));
+    TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dA_shards), s.t));
+    TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dB_shards), s.t));
+    TPMLP_TRY(check_ptr(db1));
+    TPMLP_TRY(check_ptr(db2));
+    if (s.T > 0) {
+        TPMLP_TRY(check_ptrs(dZ, s.chunks));
+        TPMLP_TRY(check_ptrs(X, s.chunks));
+        TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dX), s.chunks));
+        TPMLP_TRY(check_ptr(workspace));
+    }
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s.T == 0) {
+        const size_t wbytes = static_cast<size_t>(s.h) * s.fi * sizeof(float);
+        for (int i = 0; i < s.t; ++i) {
+            TPMLP_CUDA(cudaMemsetAsync(dA_shards[i], 0, wbytes, st));
+            TPMLP_CUDA(cudaMemsetAsync(dB_shards[i], 0, wbytes, st));
+        }
+        TPMLP_CUDA(cudaMemsetAsync(db1, 0, static_cast<size_t>(s.f) * sizeof(float), st));
+        TPMLP_CUDA(cudaMemsetAsync(db2, 0, static_cast<size_t>(s.h) * sizeof(float), st));
+        return TPMLP_OK;
+    }
+    const Layout L = layout_of(*dims);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const void* Y = ws + L.y;
+    const void* H = ws + L.h;
+    const void* dY = ws + L.dy;
+
+    // dY_i = (dZ.B_i^T) * GeLU'(Y_i): t groups, M = T, N = fi, K = h
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_kmajor(&p.a_map[j], dZ[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_ROW;
+        p.a_rows_per_map = s.Tc;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) {
+            p.out0[i] = const_cast<void*>(shard_ptr(dY, i, s));
+            p.in0[i] = shard_ptr(Y, i, s);
+        }
+        p.ld_out = s.fi;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
+                         [&] { return launch_dgrad_h(p, grid_for(p, *dev), st); }));
+    }
+    // dX = sum_i dY_i.A_i^T: M = T, N = h, K = fi per segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_kmajor(&p.a_map[i], shard_ptr(dY, i, s), s.fi, s.T, BM))
+                return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN)) return TPMLP_ERR_UNSUPPORTED;
+        }
+        p.a_part = PART_KSEG;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int j = 0; j < s.chunks; ++j) p.out0[j] = dX[j];
+        p.ld_out = s.h;
+        p.out_part = PART_ROW;
+        p.out_rows_per_part = s.Tc;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
+                         [&] { return launch_dgrad_x(p, grid_for(p, *dev), st); }));
+    }
+    // dB_i = H_i^T.dZ: t groups, M = fi, N = h, K = Tc per chunk segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.fi, s.h, s.Tc, s.t, s.chunks);
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_GROUP;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) p.out0[i] = dB_shards[i];
+        p.ld_out = s.h;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
+                         [&] { return launch_wgrad(p, grid_for(p, *dev), st); }));
+    }
+    // dA_i = X^T.dY_i: t groups, M = h, N = fi, K = Tc per chunk segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.h, s.fi, s.Tc, s.t, s.chunks);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_KSEG;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) p.out0[i] = dA_shards[i];
+        p.ld_out = s.fi;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
+                         [&] { return launch_wgrad(p, grid_for(p, *dev), st); }));
+    }
+    // db1 = column sums of dY (per shard block), db2 = column sums of dZ
+    {
+        ColsumParams c1;
+        std::memset(&c1, 0, sizeof(c1));
+        for (int i = 0; i < s.t; ++i) c1.src[i] = shard_ptr(dY, i, s);
+        c1.nparts = s.t;
+        c1.rows_per_part = s.T;
+        c1.ncols = s.fi;
+        c1.mode = CS_COLS_CONCAT;
+        c1.out = static_cast<float*>(db1);
+        c1.partial = reinterpret_cast<float*>(ws + L.part1);
+        const dim3 g1 = colsum_plan(c1, dev->sm_count);
+        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c1.splits > 1 ? 2 : 1, st,
+                         [&] { return launch_colsum(c1, g1, st, nullptr); }));
+
+        ColsumParams c2;
+        std::memset(&c2, 0, sizeof(c2));
+        for (int j = 0; j < s.chunks; ++j) c2.src[j] = dZ[j];
+        c2.nparts = s.chunks;
+        c2.rows_per_part = s.Tc;
+        c2.ncols = s.h;
+        c2.mode = CS_ROWS_CONCAT;
+        c2.out = static_cast<float*>(db2);
+        c2.partial = reinterpret_cast<float*>(ws + L.part2);
+        const dim3 g2 = colsum_plan(c2, dev->sm_count);
+        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c2.splits > 1 ? 2 : 1, st,
+                         [&] { return launch_colsum(c2, g2, st, nullptr); }));
+    }
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_sync_check(void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TPMLP_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return TPMLP_ERR_CUDA;
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TPMLP_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(dev->err, 0, sizeof(word)) != cudaSuccess) return TPMLP_ERR_CUDA;
+        return TPMLP_ERR_TIMEOUT;
+    }
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b, void* c,
+                                                   uint64_t timeout_ns, void* stream) {
+    TPMLP_TRY(check_ptr(a));
+    TPMLP_TRY(check_ptr(b));
+    TPMLP_TRY(check_ptr(c));
+    if (timeout_ns == 0) return TPMLP_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    GemmParams p;
+    base_params(p, *dev, BM, BN, BK, 1, 1);
+    if (!encode_kmajor(&p.a_map[0], a, BK, BM, BM)) return TPMLP_ERR_UNSUPPORTED;
+    if (!encode_kmajor(&p.b_map[0], b, BK, BN, BN)) return TPMLP_ERR_UNSUPPORTED;
+    p.a_part = p.b_part = PART_SINGLE;
+    p.a_rows_per_map = p.b_rows_per_map = 0;
+    p.out0[0] = c;
+    p.ld_out = BN;
+    p.out_part = PART_GROUP;
+    p.out_rows_per_part = 0;
+    p.timeout_ns = timeout_ns;
+    p.stall_producer = 1;
+    TPMLP_CUDA(launch_dgrad_x(p, 1, st));
+    return tpmlp_sync_check(stream);
+}
+
+TPMLP_API tpmlp_status tpmlp_profile_begin(int capacity) {
+    if (capacity <= 0) return TPMLP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : g_prof_pool) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g_prof_pool.assign(static_cast<size_t>(capacity), ProfRec{0, 0, nullptr, nullptr});
+    for (auto& r : g_prof_pool) {
+        if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess)
+            return TPMLP_ERR_CUDA;
+    }
+    g_prof_used = 0;
+    g_prof_on = true;
+    return TPMLP_OK;
+}
+
+TPMLP_API int tpmlp_profile_end(double* ms, int* launches, int nkinds) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return -1;
+    g_prof_on = false;
+    for (int k = 0; k < nkinds; ++k) {
+        if (ms) ms[k] = 0.0;
+        if (launches) launches[k] = 0;
+    }
+    int n = 0;
+    bool ok = true;
+    for (size_t i = 0; i < g_prof_used; ++i) {
+        ProfRec& r = g_prof_pool[i];
+        if (cudaEventSynchronize(r.b) != cudaSuccess) {
+            ok = false;
+            continue;
+        }
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+            ok = false;
+            continue;
+        }
+        if (r.kind >= 0 && r.kind < nkinds) {
+            if (ms) ms[r.kind] += t;
+            if (launches) launches[r.kind] += r.kernels;
+        }
+        ++n;
+    }
+    for (auto& r : g_prof_pool) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g_prof_pool.clear();
+    g_prof_used = 0;
+    return ok ? n : -1;
+}
+
+TPMLP_API const char* tpmlp_kernel_name(int kind) {
+    switch (kind) {
+        case TPMLP_KERNEL_COLUMN_FWD: return "column_fwd";
+        case TPMLP_KERNEL_ROW_FWD: return "row_fwd";
+        case TPMLP_KERNEL_DGRAD_H: return "dgrad_h";
+        case TPMLP_KERNEL_DGRAD_X: return "dgrad_x";
+        case TPMLP_KERNEL_WGRAD_B: return "wgrad_b";
+        case TPMLP_KERNEL_WGRAD_A: return "wgrad_a";
+        case TPMLP_KERNEL_BIAS_GRAD: return "bias_grad";
+    }
+    return "unknown";
+}

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, it
+exports every function include/tpmlp.h declares, argument validation returns
+the documented status codes before touching the device, and the product path
+never reaches the oracle."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+PKG = os.path.join(ROOT, "tensor_transformer_mlp_gemm_gb300")
+
+
+@pytest.fixture(scope="module")
+def binding():
+    from tensor_transformer_mlp_gemm_gb300.build import build
+    build()
+    from tensor_transformer_mlp_gemm_gb300 import binding as b
+    return b
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tpmlp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = _declared_functions()
+    for must in ("tpmlp_forward", "tpmlp_backward", "tpmlp_workspace_bytes", "tpmlp_sync_check"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(binding):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (tpmlp_\w+)", out))
+    declared = set(_declared_functions())
+    assert declared <= exported, declared - exported
+    # nothing else leaks from the library's C surface
+    assert exported == declared
+    assert set(binding.EXPORTED) == declared
+    lib = binding.library()
+    for name in declared:
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(binding):
+    for s in range(5):
+        assert binding.tpmlp_status_string(s)
+    assert binding.tpmlp_status_string(99) == "unknown status"
+    assert [binding.tpmlp_kernel_name(k) for k in range(binding.KERNEL_KINDS)] == [
+        "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad"]
+
+
+def test_workspace_bytes(binding):
+    d = binding.make_dims(2048, 12288, 49152, 8, 1)
+    n = binding.tpmlp_workspace_bytes(d)
+    act = 2048 * 49152 * 2
+    assert n >= 3 * act
+    y, h, dy = binding.tpmlp_workspace_layout(d)
+    assert (y, h, dy) == (0, act, 2 * act)
+    assert binding.tpmlp_workspace_bytes(binding.make_dims(128, 100, 256, 2)) == 0  # invalid
+    assert binding.tpmlp_workspace_bytes(binding.make_dims(0, 64, 256, 2)) > 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _fwd(binding, dims, t=None, X=None, A=None, b1=FAKE, B=None, b2=FAKE, Z=None, ws=FAKE):
+    n, tt = dims.seq_chunks, dims.t
+    X = X if X is not None else [FAKE] * n
+    Z = Z if Z is not None else [FAKE] * n
+    A = A if A is not None else [FAKE] * tt
+    B = B if B is not None else [FAKE] * tt
+    lib = binding.library()
+    arr = lambda xs: (ctypes.c_void_p * max(len(xs), 1))(*xs)
+    return lib.tpmlp_forward(ctypes.byref(dims), arr(X), arr(A), b1, arr(B), b2,
+                             dims.t if t is None else t, arr(Z), ws, None)
+
+
+def test_forward_validation_codes(binding):
+    mk = binding.make_dims
+    INV, UNS = binding.TPMLP_ERR_INVALID_ARG, binding.TPMLP_ERR_UNSUPPORTED
+    assert _fwd(binding, mk(256, 256, 1024, 2), t=4) == INV          # t mismatch
+    assert _fwd(binding, mk(256, 256, 1000, 3)) == INV              # t does not divide f
+    assert _fwd(binding, mk(-1, 256, 1024, 2)) == INV               # negative tokens
+    assert _fwd(binding, mk(256, 0, 1024, 2)) == INV                # empty hidden
+    assert _fwd(binding, mk(256, 100, 1024, 2)) == UNS              # h not a multiple of 8
+    assert _fwd(binding, mk(256, 256, 1044, 2)) == UNS              # fi not a multiple of 8
+    assert _fwd(binding, mk(256, 256, 1024, 16)) == UNS             # more than 8 shards
+    assert _fwd(binding, mk(384, 256, 1024, 2, 2)) == UNS           # chunk of 192 rows
+    assert _fwd(binding, mk(302, 256, 1024, 2, 4)) == INV           # chunks do not divide T
+    assert _fwd(binding, mk(256, 256, 1024, 2), b1=None) == INV     # null bias
+    assert _fwd(binding, mk(256, 256, 1024, 2), b1=FAKE + 2) == UNS  # misaligned bias
+    assert _fwd(binding, mk(256, 256, 1024, 2), A=[FAKE, None]) == INV
+    assert _fwd(binding, mk(256, 256, 1024, 2), B=[FAKE, FAKE + 8]) == UNS
+    assert _fwd(binding, mk(256, 256, 1024, 2), ws=None) == INV
+    assert _fwd(binding, mk(256, 256, 1024, 2), Z=[None]) == INV
+    assert binding.library().tpmlp_forward(None, None, None, None, None, None, 1, None, None,
+                                           None) == INV
+
+
+def test_backward_validation_codes(binding):
+    lib = binding.library()
+    d = binding.make_dims(256, 256, 1024, 2)
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    two, one = [FAKE, FAKE], [FAKE]
+    INV, UNS = binding.TPMLP_ERR_INVALID_ARG, binding.TPMLP_ERR_UNSUPPORTED
+    assert lib.tpmlp_backward(ctypes.byref(d), arr(one), arr(one), arr(two), arr(two), FAKE,
+                              arr(one), arr([FAKE, None]), FAKE, arr(two), FAKE, None) == INV
+    assert lib.tpmlp_backward(ctypes.byref(d), arr(one), arr(one), arr(two), arr(two), FAKE,
+                              arr(one), arr(two), FAKE + 4, arr(two), FAKE, None) == UNS
+    assert lib.tpmlp_backward(ctypes.byref(d), arr([None]), arr(one), arr(two), arr(two), FAKE,
+                              arr(one), arr(two), FAKE, arr(two), FAKE, None) == INV
+
+
+def test_set_timeout_and_profile_args(binding):
+    lib = binding.library()
+    assert lib.tpmlp_set_wait_timeout_ns(0) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_profile_begin(0) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_profile_end(None, None, 0) == -1  # not profiling
+
+
+def test_product_path_never_imports_the_oracle():
+    for dirpath, _, files in os.walk(PKG):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
+                assert "liboracle" not in text and "oracle.c" not in text, fn
