@@ -36,15 +36,42 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt_175b")
+    ap.add_argument("--tokens", type=int, help="override the workload's token count")
+    ap.add_argument("--hidden", type=int, help="override h")
+    ap.add_argument("--ffn", type=int, help="override f")
+    ap.add_argument("--t", type=int, help="override the shard count")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
+
+
+def pick_workload(args):
+    """The named workload, with any size overrides applied (for profiling
+    smaller cases of the same kernels)."""
+    from dataclasses import replace
+    from tensor_transformer_mlp_gemm_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    over = {}
+    if args.tokens is not None:
+        over.update(micro_batch=1, seq=args.tokens)
+    if args.hidden is not None:
+        over["hidden"] = args.hidden
+    if args.ffn is not None:
+        over["ffn"] = args.ffn
+    if args.t is not None:
+        over["t"] = args.t
+        over["seq_chunks"] = min(w.seq_chunks, args.t)
+    if over:
+        w = replace(w, name=w.name + "(" + ",".join(f"{k}={v}" for k, v in over.items()) + ")",
+                    **over)
+    return w
 
 
 def load_peaks():
@@ -227,13 +254,13 @@ def max_over_ranks(dist, torch, x: float) -> float:
 
 def run_reference(args, torch):
     """The oracle arm: fp64 CPU oracle, rank 0 only, bounded token samples."""
-    from tensor_transformer_mlp_gemm_gb300.inputs import WORKLOADS, make_inputs
+    from tensor_transformer_mlp_gemm_gb300.inputs import make_inputs
     dist, rank, world, _ = dist_setup(torch)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     inputs = make_inputs(w, 0)
     smp = OracleSample(w, inputs)
     per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
@@ -272,11 +299,11 @@ def run_ours(args, torch):
         dist.barrier()
     from tensor_transformer_mlp_gemm_gb300 import binding
     from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
-    from tensor_transformer_mlp_gemm_gb300.inputs import WORKLOADS, make_inputs
+    from tensor_transformer_mlp_gemm_gb300.inputs import make_inputs
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
+    w = pick_workload(args)
     inputs = make_inputs(w, 0)
     blk = DeviceBlock(w, inputs, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -362,25 +389,28 @@ def run_ours(args, torch):
         for d, s in zip(hdX, blk.dX):
             d.copy_(s, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    barrier(dist, torch)
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e3.record(stream)
-    barrier(dist, torch)
-    st = binding.tpmlp_sync_check(stream)
-    if st != binding.TPMLP_OK:
-        raise RuntimeError(f"e2e loop failed: {binding.tpmlp_status_string(st)}")
-    ms_e2e = max_over_ranks(dist, torch, e2.elapsed_time(e3))
-    e2e = {"value": flops_step * args.e2e_steps * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": sum(x.numel() * 2 for x in hX + hdZ),
-           "d2h_bytes_per_step": sum(x.numel() * 2 for x in hZ + hdX),
-           "tokens_per_s": T * args.e2e_steps * world / (ms_e2e / 1e3),
-           "steps": args.e2e_steps}
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            e2e_step()
+        barrier(dist, torch)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e3.record(stream)
+        barrier(dist, torch)
+        st = binding.tpmlp_sync_check(stream)
+        if st != binding.TPMLP_OK:
+            raise RuntimeError(f"e2e loop failed: {binding.tpmlp_status_string(st)}")
+        ms_e2e = max_over_ranks(dist, torch, e2.elapsed_time(e3))
+        e2e = {"value": flops_step * args.e2e_steps * world / (ms_e2e / 1e3) / 1e12,
+               "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(x.numel() * 2 for x in hX + hdZ),
+               "d2h_bytes_per_step": sum(x.numel() * 2 for x in hZ + hdX),
+               "tokens_per_s": T * args.e2e_steps * world / (ms_e2e / 1e3),
+               "steps": args.e2e_steps}
 
     if rank == 0:
         cpu = None
