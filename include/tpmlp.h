@@ -162,6 +162,31 @@ tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);
 tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b, void* c,
                                          uint64_t timeout_ns, void* stream);
 
+/* Column sums of one bf16 matrix [rows, cols] into fp32 out[cols] -- the
+ * reduction tpmlp_backward uses for its bias gradients (db2 is the column
+ * sums of dZ) -- for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this call; it exists for the library's users.
+ *
+ * Who needs it: tpmlp_backward takes its scratch from a caller-allocated
+ * workspace.  A caller embedded in another runtime whose device memory is
+ * owned by that runtime's pool cannot add a cudaMalloc of its own (it would
+ * escape the pool's budget, and cudaFree synchronises the whole device); a
+ * latency-critical loop may forbid allocation after start-up.  This call
+ * allocates nothing: it keeps its partial sums in a static 4 MiB device
+ * array (1,048,576 floats) inside the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   src   device bf16 [rows, cols], row-major, 16-byte aligned
+ *   rows  >= 0 (rows = 0 writes zeros), below 2^31
+ *   cols  multiple of 8, at most 1,048,576; larger returns TPMLP_ERR_UNSUPPORTED
+ *   out   device fp32 [cols], 16-byte aligned, overwritten
+ * The first call on a device does a one-time set-up (looks up the array's
+ * device address); make that first call before any stream capture.  All
+ * calls on a device share the array and the last call's contents stay in it;
+ * nothing in it needs clearing, but calls that overlap on the GPU (unordered
+ * streams) race on it.  Asynchronous on `stream`, like every other call. */
+tpmlp_status tpmlp_column_sums_noalloc(const void* src, int64_t rows, int64_t cols, void* out,
+                                       void* stream);
+
 /* Kernel-level timing.  Between tpmlp_profile_begin and tpmlp_profile_end
  * the library records a CUDA event pair on the launch stream around each of
  * its kernel launches (at most `capacity` launches).  tpmlp_profile_end

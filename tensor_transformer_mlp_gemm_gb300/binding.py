@@ -34,7 +34,7 @@ EXPORTED = (
     "tpmlp_workspace_bytes", "tpmlp_workspace_layout", "tpmlp_forward", "tpmlp_backward",
     "tpmlp_status_string", "tpmlp_sync_check", "tpmlp_set_wait_timeout_ns",
     "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
-    "tpmlp_kernel_name",
+    "tpmlp_kernel_name", "tpmlp_column_sums_noalloc",
 )
 
 
@@ -77,6 +77,8 @@ _lib.tpmlp_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINT
                                    ctypes.c_int]
 _lib.tpmlp_kernel_name.restype = ctypes.c_char_p
 _lib.tpmlp_kernel_name.argtypes = [ctypes.c_int]
+_lib.tpmlp_column_sums_noalloc.restype = ctypes.c_int
+_lib.tpmlp_column_sums_noalloc.argtypes = [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp]
 
 
 def library_path() -> str:
@@ -177,3 +179,10 @@ def tpmlp_profile_end() -> tuple[dict, dict]:
     names = [tpmlp_kernel_name(k) for k in range(KERNEL_KINDS)]
     return ({names[k]: ms[k] for k in range(KERNEL_KINDS)},
             {names[k]: cnt[k] for k in range(KERNEL_KINDS)})
+
+
+def tpmlp_column_sums_noalloc(src, rows: int, cols: int, out, stream=None) -> int:
+    """Column sums of bf16 src [rows, cols] into fp32 out [cols] with no device
+    allocation (library-owned static scratch).  Returns the status."""
+    return int(_lib.tpmlp_column_sums_noalloc(_ptr(src), int(rows), int(cols), _ptr(out),
+                                              _stream(stream)))
