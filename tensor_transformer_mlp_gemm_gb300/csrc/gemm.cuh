@@ -163,6 +163,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk) {
 }
 
 // ---- epilogue ----------------------------------------------------------------------
+// Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter) and walks
+// the tile's columns 32 at a time: tcgen05.ld -> fused elementwise work in
+// fp32 -> one row per lane written into a swizzled 32 x 32 staging buffer ->
+// one lane issues a TMA bulk tensor store.  The store clips rows and columns
+// outside the tensor, so ragged edges need no masks.  Two staging buffers
+// per warp let the stores of chunk c-1 drain while chunk c is being staged.
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -178,47 +184,53 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&f)[8]) {
     }
 }
 
-// One thread: row m, columns [n, n+32) of the tile, accumulator values v.
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int g, int m, int n,
-                                               const uint32_t (&v)[32]) {
-    if (m >= p.M) return;
-    int part = g;
-    long long row = m;
-    if (p.out_part == PART_ROW) {
-        part = m / p.out_rows_per_part;
-        row = m - static_cast<long long>(part) * p.out_rows_per_part;
+// Row `r` (32 fp32 values) into a 32 x 32 fp32 box staged with the 128-byte
+// swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8).
+__device__ __forceinline__ void stage_row_f32(uint8_t* buf, int r, const float (&x)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float4 v = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+        *reinterpret_cast<float4*>(buf + r * 128 + ((c ^ (r & 7)) << 4)) = v;
     }
-    const long long off = row * p.ld_out + n;
+}
 
-    if constexpr (EPI == EPI_F32) {
-        float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out0[part]) + off);
+// Row `r` (32 bf16 values) into a 32 x 32 bf16 box staged with the 64-byte
+// swizzle: 16-byte chunk c of row r lives at chunk c ^ ((r / 2) % 4).
+__device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int r, const float (&x)[32]) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            if (n + 4 * q < p.N)
-                o[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
-    } else {
-        float x[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+    for (int c = 0; c < 4; ++c) {
+        const float* a = x + 8 * c;
+        uint4 v = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                             pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+        *reinterpret_cast<uint4*>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = v;
+    }
+}
 
-        if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS) {
-            const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(p.bias) + n +
-                                     (EPI == EPI_BIAS_GELU ? g * p.bias_group_stride : 0);
+// Elementwise work on one thread's 32 values: row m, columns [n, n + 32).
+template <int EPI>
+__device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int part, long long row,
+                                              int m, int n, float (&x)[32], float (&x2)[32]) {
+    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS) {
+        const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(p.bias) + n +
+                                 (EPI == EPI_BIAS_GELU ? g * p.bias_group_stride : 0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (n + 8 * q < p.N) {
-                    float bf[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(b + 8 * q), bf);
+        for (int q = 0; q < 4; ++q) {
+            if (n + 8 * q < p.N) {
+                float bf[8];
+                unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(b + 8 * q)), bf);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) x[8 * q + j] += bf[j];
-                }
+                for (int j = 0; j < 8; ++j) x[8 * q + j] += bf[j];
             }
         }
-        if constexpr (EPI == EPI_DGELU) {
-            const __nv_bfloat16* y = static_cast<const __nv_bfloat16*>(p.in0[part]) + off;
+        if constexpr (EPI == EPI_BIAS_GELU) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x2[j] = gelu_f(x[j]);
+        }
+    }
+    if constexpr (EPI == EPI_DGELU) {
+        if (m < p.M) {
+            const __nv_bfloat16* y =
+                static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (n + 8 * q < p.N) {
@@ -226,29 +238,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams& p, int g, int m
                     unpack_bf16x8(*reinterpret_cast<const uint4*>(y + 8 * q), yf);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) x[8 * q + j] *= gelu_grad_f(yf[j]);
-                }
-            }
-        }
-        uint4* o0 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0[part]) + off);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (n + 8 * q < p.N) {
-                const float* a = x + 8 * q;
-                o0[q] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                                   pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
-            }
-        }
-        if constexpr (EPI == EPI_BIAS_GELU) {
-            uint4* o1 =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out1[part]) + off);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (n + 8 * q < p.N) {
-                    const float* a = x + 8 * q;
-                    o1[q] = make_uint4(pack_bf16x2(gelu_f(a[0]), gelu_f(a[1])),
-                                       pack_bf16x2(gelu_f(a[2]), gelu_f(a[3])),
-                                       pack_bf16x2(gelu_f(a[4]), gelu_f(a[5])),
-                                       pack_bf16x2(gelu_f(a[6]), gelu_f(a[7])));
                 }
             }
         }
@@ -262,8 +251,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* bar_area = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    uint8_t* epi_area = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
+    uint8_t* bar_area = epi_area + EPI_STAGE_BYTES;
+    const uint32_t epi0 = base + STAGES * STAGE_BYTES;
+    const uint32_t bar0 = epi0 + EPI_STAGE_BYTES;
     const uint32_t bar_full = bar0;                      // [STAGES]
     const uint32_t bar_empty = bar0 + 8 * STAGES;        // [STAGES]
     const uint32_t bar_tfull = bar0 + 16 * STAGES;       // [2]
@@ -392,6 +383,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
         // ---------------- epilogue (warps 2..5) ----------------
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
+        uint8_t* stage_buf = epi_area + (warp - 2) * (2 * EPI_BUF_BYTES);
+        const uint32_t stage_u32 = epi0 + (warp - 2) * (2 * EPI_BUF_BYTES);
+        int chunk_seq = 0;
         int lt = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++lt) {
             int g, m0, n0;
@@ -403,18 +397,57 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
             if (__any_sync(0xffffffffu, !ok)) break;
             __syncwarp();
             ptx::tc_fence_after();
+            // output map and row coordinate of this warp's 32 rows
+            int part = g;
+            int y0 = m0 + quarter * 32;
+            if (p.out_part == PART_ROW) {
+                part = m0 / p.out_rows_per_part;
+                y0 -= part * p.out_rows_per_part;
+            }
+            const int m = m0 + row;
+            const long long in_row = static_cast<long long>(y0) + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                 uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(taddr + c * 32, v);
+                ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                 ptx::tmem_ld_wait();
-                if (n0 + c * 32 < p.N) epilogue_chunk<EPI>(p, g, m0 + row, n0 + c * 32, v);
+                const int n = n0 + c * EPI_CHUNK;
+                if (n >= p.N) continue;  // whole chunk outside the tensor (warp-uniform)
+                float x[32], x2[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+                epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                // staging buffer of this chunk: free once the store issued two
+                // chunks ago has finished reading it
+                const int b = chunk_seq & 1;
+                ++chunk_seq;
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                uint8_t* buf = stage_buf + b * EPI_BUF_BYTES;
+                if constexpr (EPI == EPI_F32) {
+                    stage_row_f32(buf, lane, x);
+                } else {
+                    stage_row_bf16(buf, lane, x);
+                    if constexpr (EPI == EPI_BIAS_GELU) stage_row_bf16(buf + 2048, lane, x2);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t sb = stage_u32 + b * EPI_BUF_BYTES;
+                    ptx::tma_store_2d(&p.out_map[part], sb, n, y0);
+                    if constexpr (EPI == EPI_BIAS_GELU)
+                        ptx::tma_store_2d(&p.out_map[MAX_MAPS + part], sb + 2048, n, y0);
+                    ptx::bulk_commit_group();
+                }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_tempty + 8 * acc);
         }
+        // every store must have finished before the CTA leaves
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();

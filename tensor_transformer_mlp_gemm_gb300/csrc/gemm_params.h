@@ -19,7 +19,11 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
-constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_CHUNK = 32;                 // accumulator columns per epilogue step
+constexpr int EPI_BUF_BYTES = 4096;           // one staged 32 x 32 chunk (fp32, or 2 x bf16)
+constexpr int EPI_STAGE_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // double-buffered per warp
+constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES;
 constexpr int MAX_MAPS = 8;
 constexpr int MN_CHUNK = 64;                      // elements per 128-byte row
 constexpr int MN_CHUNK_BYTES = MN_CHUNK * BK * 2;  // one MN-major box [BK][64]
@@ -32,12 +36,14 @@ enum Part : int {
     PART_ROW = 3      // map row0 / rows_per_map (token chunks); K over all segments
 };
 
+// Output i of a tile goes through out_map[i] (first output) and
+// out_map[MAX_MAPS + i] (second output), i = group or token chunk.
 enum Epi : int {
-    EPI_BIAS_GELU = 1,  // out0 = bf16(acc + bias), out1 = bf16(GeLU(acc + bias))
-    EPI_BIAS = 2,       // out0 = bf16(acc + bias)
-    EPI_DGELU = 3,      // out0 = bf16(acc * GeLU'(in0))
-    EPI_BF16 = 4,       // out0 = bf16(acc)
-    EPI_F32 = 5         // out0 = acc (fp32)
+    EPI_BIAS_GELU = 1,  // out 1 = bf16(acc + bias), out 2 = bf16(GeLU(acc + bias))
+    EPI_BIAS = 2,       // out 1 = bf16(acc + bias)
+    EPI_DGELU = 3,      // out 1 = bf16(acc * GeLU'(in0))
+    EPI_BF16 = 4,       // out 1 = bf16(acc)
+    EPI_F32 = 5         // out 1 = acc (fp32)
 };
 
 // Error-word bits (which role gave up).
@@ -51,12 +57,12 @@ struct GemmParams {
     int a_part, b_part;
     int a_rows_per_map, b_rows_per_map;
     int mtiles, ntiles, total_tiles, band;
-    // epilogue
-    void* out0[MAX_MAPS];
-    void* out1[MAX_MAPS];
+    // epilogue: TMA store maps (box 32 x 32, 128-byte swizzle for fp32,
+    // 64-byte swizzle for bf16) and the saved pre-activation for EPI_DGELU
+    CUtensorMap out_map[2 * MAX_MAPS];
     const void* in0[MAX_MAPS];
     const void* bias;
-    long long ld_out;        // leading dimension of out0/out1/in0 (elements)
+    long long ld_in;         // leading dimension of in0 (elements)
     int out_part;            // PART_GROUP or PART_ROW
     int out_rows_per_part;   // rows per output chunk for PART_ROW
     int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU)

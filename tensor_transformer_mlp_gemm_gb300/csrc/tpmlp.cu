@@ -151,6 +151,22 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K) 
     return encode_bf16(m, ptr, rows, K, rows, MN_CHUNK, BK);
 }
 
+// Epilogue store map: row-major [rows, cols] output, box 32 x 32; fp32 boxes
+// are staged with the 128-byte swizzle, bf16 boxes with the 64-byte swizzle.
+bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, bool f32) {
+    const uint64_t esize = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * esize};
+    cuuint32_t box[2] = {EPI_CHUNK, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- workspace ---------------------------------------------------------------------------
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -230,11 +246,8 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     p.stall_producer = 0;
     p.bias = nullptr;
     p.bias_group_stride = 0;
-    for (int i = 0; i < MAX_MAPS; ++i) {
-        p.out0[i] = nullptr;
-        p.out1[i] = nullptr;
-        p.in0[i] = nullptr;
-    }
+    p.ld_in = 0;
+    for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
 }
 
 int grid_for(const GemmParams& p, const DeviceInfo& dev) {
@@ -338,10 +351,10 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
-            p.out0[i] = const_cast<void*>(shard_ptr(Y, i, s));
-            p.out1[i] = const_cast<void*>(shard_ptr(H, i, s));
+            if (!encode_out(&p.out_map[i], shard_ptr(Y, i, s), s.fi, s.T, false) ||
+                !encode_out(&p.out_map[MAX_MAPS + i], shard_ptr(H, i, s), s.fi, s.T, false))
+                return TPMLP_ERR_UNSUPPORTED;
         }
-        p.ld_out = s.fi;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         p.bias = b1;
@@ -361,8 +374,8 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.a_part = PART_KSEG;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int j = 0; j < s.chunks; ++j) p.out0[j] = Z[j];
-        p.ld_out = s.h;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_out(&p.out_map[j], Z[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
         p.bias = b2;
@@ -423,10 +436,11 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
-            p.out0[i] = const_cast<void*>(shard_ptr(dY, i, s));
+            if (!encode_out(&p.out_map[i], shard_ptr(dY, i, s), s.fi, s.T, false))
+                return TPMLP_ERR_UNSUPPORTED;
             p.in0[i] = shard_ptr(Y, i, s);
         }
-        p.ld_out = s.fi;
+        p.ld_in = s.fi;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
@@ -444,8 +458,8 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.a_part = PART_KSEG;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int j = 0; j < s.chunks; ++j) p.out0[j] = dX[j];
-        p.ld_out = s.h;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_out(&p.out_map[j], dX[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
@@ -463,8 +477,9 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
             if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i) p.out0[i] = dB_shards[i];
-        p.ld_out = s.h;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_out(&p.out_map[i], dB_shards[i], s.h, s.fi, true))
+                return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
@@ -482,8 +497,9 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
                 return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i) p.out0[i] = dA_shards[i];
-        p.ld_out = s.fi;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_out(&p.out_map[i], dA_shards[i], s.fi, s.h, true))
+                return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
@@ -551,8 +567,7 @@ TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b,
     if (!encode_kmajor(&p.b_map[0], b, BK, BN, BN)) return TPMLP_ERR_UNSUPPORTED;
     p.a_part = p.b_part = PART_SINGLE;
     p.a_rows_per_map = p.b_rows_per_map = 0;
-    p.out0[0] = c;
-    p.ld_out = BN;
+    if (!encode_out(&p.out_map[0], c, BN, BM, false)) return TPMLP_ERR_UNSUPPORTED;
     p.out_part = PART_GROUP;
     p.out_rows_per_part = 0;
     p.timeout_ns = timeout_ns;
