@@ -21,7 +21,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/tpmlp.h"
+#include "tpmlp.h"
 #include "colsum.cuh"
 
 #define TPMLP_NOALLOC_API extern "C" __attribute__((visibility("default")))

@@ -30,7 +30,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/tpmlp.h"
+#include "tpmlp.h"
 #include "colsum.cuh"
 #include "gemm_params.h"
 
