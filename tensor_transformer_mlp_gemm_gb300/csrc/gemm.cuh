@@ -21,7 +21,14 @@
 // [K, rows]); the weight-gradient GEMMs contract over tokens and read both
 // operands MN-major straight from the token-major activations.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+// Clusters of 2 CTAs (one CTA per SM) work on 256 x 256 cluster tiles: CTA r
+// computes rows [128 r, 128 r + 128) with tcgen05.mma.cta_group::1, loads its
+// own 128 rows of A, and loads half of the shared B tile with a TMA multicast
+// that lands in both CTAs.  Each SM therefore pulls 32 KB instead of 48 KB
+// from L2 per K step.  A stage is free again only when BOTH CTAs' MMAs have
+// consumed it (each MMA releases the stage in both CTAs).
+//
+// CTA layout (192 threads, one CTA per SM, persistent over cluster tiles):
 //   warp 0      TMA producer (one elected thread): A and B tiles into a
 //               STAGES-deep shared-memory ring, completion on mbarriers
 //   warp 1      owns the tensor memory; one elected thread issues
@@ -117,17 +124,23 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     const int ntg = r / rows_here;
     g = ntg / p.ntiles;
     n0 = (ntg - g * p.ntiles) * BN;
-    m0 = mt * BM;
+    m0 = mt * CLUSTER_M;
 }
 
 // ---- operand loads -----------------------------------------------------------------
 // K-major operand: tensor [rows, K] (inner K), box {BK, ROWS}; one copy.
 // MN-major operand: tensor [K, rows] (inner rows), box {64, BK}; ROWS/64
 // copies, box j landing at dst + j * MN_CHUNK_BYTES.
-template <bool MN, int ROWS>
+// HALF (shared B tile): this CTA loads only half `half` of the rows and
+// multicasts it to both CTAs of the cluster (K-major: box {BK, ROWS/2}).
+// PART_ROW: a tile whose rows start past the last token chunk (the second
+// CTA of a cluster tile when T is not a multiple of 256) reads the last
+// chunk's map at out-of-range rows, which TMA fills with zeros; the map index
+// never leaves the encoded maps.
+template <bool MN, int ROWS, bool HALF>
 __device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, int rows_per_map,
-                                             int g, int s, int row0, int kc, int K, uint32_t dst,
-                                             uint32_t bar) {
+                                             int nmaps, int g, int s, int row0, int kc, int K,
+                                             uint32_t dst, uint32_t bar, int half) {
     int idx = 0, r = row0, k = s * K + kc;
     if (part == PART_GROUP) {
         idx = g;
@@ -135,16 +148,30 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, 
         idx = s;
         k = kc;
     } else if (part == PART_ROW) {
-        idx = row0 / rows_per_map;
+        idx = min(row0 / rows_per_map, nmaps - 1);
         r = row0 - idx * rows_per_map;
     }
     const CUtensorMap* m = maps + idx;
-    if constexpr (!MN) {
-        ptx::tma_load_2d(dst, m, k, r, bar);
-    } else {
+    if constexpr (!HALF) {
+        if constexpr (!MN) {
+            ptx::tma_load_2d(dst, m, k, r, bar);
+        } else {
 #pragma unroll
-        for (int j = 0; j < ROWS / MN_CHUNK; ++j)
-            ptx::tma_load_2d(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
+            for (int j = 0; j < ROWS / MN_CHUNK; ++j)
+                ptx::tma_load_2d(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
+        }
+    } else {
+        constexpr int HROWS = ROWS / 2;
+        if constexpr (!MN) {
+            ptx::tma_load_2d_multicast(dst + half * HROWS * 128, m, k, r + half * HROWS, bar, 0x3);
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < HROWS / MN_CHUNK; ++jj) {
+                const int j = half * (HROWS / MN_CHUNK) + jj;
+                ptx::tma_load_2d_multicast(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar,
+                                           0x3);
+            }
+        }
     }
 }
 
@@ -247,7 +274,8 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
 // ---- the kernel ---------------------------------------------------------------------
 
 template <bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    tpmlp_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -265,11 +293,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 2);  // released by both CTAs' MMAs
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar_tfull + 8 * a, 1);
@@ -284,8 +315,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // both CTAs' barriers exist before any multicast or remote arrive
     ptx::tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -299,9 +332,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+            for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
                 int g, m0, n0;
                 decode_tile(p, tile, g, m0, n0);
+                const int a_row = m0 + rank * BM;
                 for (int s = 0; ok && s < p.ksegs; ++s) {
                     for (int kb = 0; kb < kblocks; ++kb) {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
@@ -313,10 +347,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
                             const uint32_t full = bar_full + 8 * stage;
                             const uint32_t sa = base + stage * STAGE_BYTES;
                             ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
-                            load_operand<A_MN, BM>(p.a_map, p.a_part, p.a_rows_per_map, g, s, m0,
-                                                   kb * BK, p.K, sa, full);
-                            load_operand<B_MN, BN>(p.b_map, p.b_part, p.b_rows_per_map, g, s, n0,
-                                                   kb * BK, p.K, sa + A_STAGE_BYTES, full);
+                            load_operand<A_MN, BM, false>(p.a_map, p.a_part, p.a_rows_per_map,
+                                                          p.a_nmaps, g, s, a_row, kb * BK, p.K,
+                                                          sa, full, 0);
+                            load_operand<B_MN, BN, true>(p.b_map, p.b_part, p.b_rows_per_map,
+                                                         p.b_nmaps, g, s, n0, kb * BK, p.K,
+                                                         sa + A_STAGE_BYTES, full, rank);
                             ++fills;
                         }
                         if (++stage == STAGES) {
@@ -326,8 +362,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
                     }
                 }
             }
-            if (!ok) {
-                // Wait for this CTA's own copies still in flight (the last
+            if (ok) {
+                // Producer tail: the peer's MMA releases each stage with an
+                // asynchronous arrive on this CTA's "empty" barrier.  Wait until
+                // every stage filled here has been released by both MMAs, so no
+                // such arrive can land after this CTA has exited.
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!wait_drain(bar_empty + 8 * stage, phase ^ 1u, p)) break;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                // Wait for the copies into this CTA still in flight (the last
                 // STAGES fills) before the CTA can leave.
                 for (long long f = (fills > STAGES ? fills - STAGES : 0); f < fills; ++f) {
                     const int st = static_cast<int>(f % STAGES);
@@ -344,7 +392,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
             uint32_t phase = 0;
             int lt = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++lt) {
+            for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
                 if (!wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p, ERR_MMA)) {
@@ -367,7 +415,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
                                          operand_desc<B_MN>(sb, k), IDESC,
                                          (kk > 0 || k > 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit(bar_empty + 8 * stage);
+                    ptx::mma_commit_multicast(bar_empty + 8 * stage, 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -387,9 +435,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
         const uint32_t stage_u32 = epi0 + (warp - 2) * (2 * EPI_BUF_BYTES);
         int chunk_seq = 0;
         int lt = 0;
-        for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++lt) {
-            int g, m0, n0;
-            decode_tile(p, tile, g, m0, n0);
+        for (int tile = cluster; tile < p.total_tiles; tile += nclusters, ++lt) {
+            int g, mp, n0;
+            decode_tile(p, tile, g, mp, n0);
+            const int m0 = mp + rank * BM;  // this CTA's first row
             const int acc = lt & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
             const bool ok = wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag, p,
@@ -400,7 +449,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
             // output map and row coordinate of this warp's 32 rows
             int part = g;
             int y0 = m0 + quarter * 32;
-            if (p.out_part == PART_ROW) {
+            if (p.out_part == PART_ROW && m0 < p.M) {
                 part = m0 / p.out_rows_per_part;
                 y0 -= part * p.out_rows_per_part;
             }
@@ -414,7 +463,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
                 ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                 ptx::tmem_ld_wait();
                 const int n = n0 + c * EPI_CHUNK;
-                if (n >= p.N) continue;  // whole chunk outside the tensor (warp-uniform)
+                if (n >= p.N || m0 >= p.M) continue;  // chunk outside the tensor (warp-uniform)
                 float x[32], x2[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
@@ -450,8 +499,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
         __syncwarp();
     }
 
+    // neither CTA leaves while the other may still multicast into it
     ptx::tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    ptx::cluster_sync();
     ptx::tc_fence_after();
     if (warp == 1) {
         __syncwarp();
@@ -459,14 +510,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) tpmlp_gemm_kernel(const __gri
     }
 }
 
-#define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)                                           \
-    cudaError_t NAME(const GemmParams& p, int grid, cudaStream_t stream) {                      \
-        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;                                          \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             GEMM_SMEM_BYTES);                                   \
-        if (e != cudaSuccess) return e;                                                          \
-        kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(p);                                \
-        return cudaGetLastError();                                                               \
+// Persistent launch: one 2-CTA cluster per cluster tile, capped at the number
+// of clusters that fit on the GPU at once (queried once per kernel variant).
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_clusters(const GemmParams& p, cudaStream_t stream) {
+    auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;
+    static int max_clusters = 0;
+    if (max_clusters == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             GEMM_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters = n;
+    }
+    const int clusters = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+    kern<<<2 * clusters, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+}
+
+#define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)               \
+    cudaError_t NAME(const GemmParams& p, cudaStream_t stream) {  \
+        return launch_clusters<A_MN, B_MN, EPI>(p, stream);       \
     }
 
 }  // namespace tpmlp

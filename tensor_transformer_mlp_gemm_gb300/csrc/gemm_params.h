@@ -9,7 +9,11 @@
 
 namespace tpmlp {
 
-constexpr int BM = 128;       // tile rows (TMEM lanes)
+// Two CTAs of a cluster own vertically adjacent 128 x 256 tiles (a 256 x 256
+// cluster tile) with the same B tile: each loads its own A and one half of B,
+// multicast into both CTAs' shared memory.
+constexpr int BM = 128;       // tile rows per CTA (TMEM lanes)
+constexpr int CLUSTER_M = 2 * BM;  // rows per cluster tile
 constexpr int BN = 256;       // tile columns (TMEM columns per accumulator)
 constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
 constexpr int STAGES = 4;
@@ -56,7 +60,8 @@ struct GemmParams {
     int groups, ksegs;
     int a_part, b_part;
     int a_rows_per_map, b_rows_per_map;
-    int mtiles, ntiles, total_tiles, band;
+    int a_nmaps, b_nmaps;   // encoded maps; PART_ROW indices are clamped to them
+    int mtiles, ntiles, total_tiles, band;  // cluster tiles of CLUSTER_M x BN
     // epilogue: TMA store maps (box 32 x 32, 128-byte swizzle for fp32,
     // 64-byte swizzle for bf16) and the saved pre-activation for EPI_DGELU
     CUtensorMap out_map[2 * MAX_MAPS];
@@ -72,16 +77,18 @@ struct GemmParams {
     int stall_producer;      // failure-detection self-test: issue no loads
 };
 
-// Launchers, one per (operand majorness, epilogue) variant.
+// Launchers, one per (operand majorness, epilogue) variant.  Each launches a
+// persistent grid of 2-CTA clusters (at most one cluster per cluster tile,
+// at most as many clusters as fit on the GPU at once).
 //   column_fwd : A K-major,  B MN-major, EPI_BIAS_GELU  (Y_i, H_i)
 //   row_fwd    : A K-major,  B MN-major, EPI_BIAS       (Z)
 //   dgrad_h    : A K-major,  B K-major,  EPI_DGELU      (dY_i)
 //   dgrad_x    : A K-major,  B K-major,  EPI_BF16       (dX)
 //   wgrad      : A MN-major, B MN-major, EPI_F32        (dA_i, dB_i)
-cudaError_t launch_column_fwd(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_row_fwd(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_dgrad_h(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_dgrad_x(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_wgrad(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_column_fwd(const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_row_fwd(const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_dgrad_h(const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_dgrad_x(const GemmParams& p, cudaStream_t stream);
+cudaError_t launch_wgrad(const GemmParams& p, cudaStream_t stream);
 
 }  // namespace tpmlp

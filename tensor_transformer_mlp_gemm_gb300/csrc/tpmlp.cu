@@ -45,7 +45,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxShards = 8;
-constexpr int kBand = 16;  // M-tiles per raster band
+constexpr int kBand = 8;   // cluster M-tiles (256 rows each) per raster band
 
 struct DeviceInfo {
     bool ready = false;
@@ -232,12 +232,15 @@ tpmlp_status check_ptr(const void* p) {
 // ---- GEMM set-up ------------------------------------------------------------------------
 void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int groups,
                  int ksegs) {
+    std::memset(&p, 0, sizeof(p));
+    p.a_nmaps = 1;
+    p.b_nmaps = 1;
     p.M = M;
     p.N = N;
     p.K = K;
     p.groups = groups;
     p.ksegs = ksegs;
-    p.mtiles = (M + BM - 1) / BM;
+    p.mtiles = (M + CLUSTER_M - 1) / CLUSTER_M;
     p.ntiles = (N + BN - 1) / BN;
     p.total_tiles = p.mtiles * p.ntiles * groups;
     p.band = p.mtiles < kBand ? p.mtiles : kBand;
@@ -248,10 +251,6 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     p.bias_group_stride = 0;
     p.ld_in = 0;
     for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
-}
-
-int grid_for(const GemmParams& p, const DeviceInfo& dev) {
-    return p.total_tiles < dev.sm_count ? p.total_tiles : dev.sm_count;
 }
 
 struct Shapes {
@@ -345,6 +344,8 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_kmajor(&p.a_map[j], X[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_ROW;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
             if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h)) return TPMLP_ERR_UNSUPPORTED;
@@ -360,7 +361,7 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.bias = b1;
         p.bias_group_stride = s.fi;
         TPMLP_CUDA(timed(TPMLP_KERNEL_COLUMN_FWD, 1, st,
-                         [&] { return launch_column_fwd(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_column_fwd(p, st); }));
     }
     // row-parallel GEMM, shard split-K + b2: M = T, N = h, K = fi per segment
     {
@@ -372,6 +373,8 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
             if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi)) return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = PART_KSEG;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.t;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
         for (int j = 0; j < s.chunks; ++j)
@@ -380,7 +383,7 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.out_rows_per_part = s.Tc;
         p.bias = b2;
         TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
-                         [&] { return launch_row_fwd(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_row_fwd(p, st); }));
     }
     return TPMLP_OK;
 }
@@ -430,9 +433,11 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_kmajor(&p.a_map[j], dZ[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_ROW;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
@@ -444,7 +449,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
-                         [&] { return launch_dgrad_h(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_dgrad_h(p, st); }));
     }
     // dX = sum_i dY_i.A_i^T: M = T, N = h, K = fi per segment
     {
@@ -453,9 +458,11 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         for (int i = 0; i < s.t; ++i) {
             if (!encode_kmajor(&p.a_map[i], shard_ptr(dY, i, s), s.fi, s.T, BM))
                 return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = PART_KSEG;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.t;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
         for (int j = 0; j < s.chunks; ++j)
@@ -463,7 +470,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
-                         [&] { return launch_dgrad_x(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_dgrad_x(p, st); }));
     }
     // dB_i = H_i^T.dZ: t groups, M = fi, N = h, K = Tc per chunk segment
     {
@@ -473,6 +480,8 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
             if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T))
                 return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_GROUP;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.chunks;
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_KSEG;
@@ -483,7 +492,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
-                         [&] { return launch_wgrad(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_wgrad(p, st); }));
     }
     // dA_i = X^T.dY_i: t groups, M = h, N = fi, K = Tc per chunk segment
     {
@@ -492,6 +501,8 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_KSEG;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
         for (int i = 0; i < s.t; ++i)
             if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T))
                 return TPMLP_ERR_UNSUPPORTED;
@@ -503,7 +514,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
-                         [&] { return launch_wgrad(p, grid_for(p, *dev), st); }));
+                         [&] { return launch_wgrad(p, st); }));
     }
     // db1 = column sums of dY (per shard block), db2 = column sums of dZ
     {
@@ -564,7 +575,7 @@ TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b,
     GemmParams p;
     base_params(p, *dev, BM, BN, BK, 1, 1);
     if (!encode_kmajor(&p.a_map[0], a, BK, BM, BM)) return TPMLP_ERR_UNSUPPORTED;
-    if (!encode_kmajor(&p.b_map[0], b, BK, BN, BN)) return TPMLP_ERR_UNSUPPORTED;
+    if (!encode_kmajor(&p.b_map[0], b, BK, BN, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
     p.a_part = p.b_part = PART_SINGLE;
     p.a_rows_per_map = p.b_rows_per_map = 0;
     if (!encode_out(&p.out_map[0], c, BN, BM, false)) return TPMLP_ERR_UNSUPPORTED;
@@ -572,7 +583,7 @@ TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b,
     p.out_rows_per_part = 0;
     p.timeout_ns = timeout_ns;
     p.stall_producer = 1;
-    TPMLP_CUDA(launch_dgrad_x(p, 1, st));
+    TPMLP_CUDA(launch_dgrad_x(p, st));
     return tpmlp_sync_check(stream);
 }
 
