@@ -21,28 +21,36 @@
 // [K, rows]); the weight-gradient GEMMs contract over tokens and read both
 // operands MN-major straight from the token-major activations.
 //
-// Clusters of 2 CTAs (one CTA per SM) work on 256 x 256 cluster tiles: CTA r
-// computes rows [128 r, 128 r + 128) with tcgen05.mma.cta_group::1, loads its
-// own 128 rows of A, and loads half of the shared B tile with a TMA multicast
-// that lands in both CTAs.  Each SM therefore pulls 32 KB instead of 48 KB
-// from L2 per K step.  A stage is free again only when BOTH CTAs' MMAs have
-// consumed it (each MMA releases the stage in both CTAs).
+// Work unit: a CTA pair (cluster of 2, one CTA per SM) owns a 256 x 256
+// output tile and computes it with tcgen05.mma.cta_group::2 (256 x 256 x 16
+// per instruction, issued by the even CTA).  Each CTA stages its own 128 rows
+// of A and its own 128 rows of B per K step (32 KB), so a 6-deep ring fits in
+// shared memory and each SM keeps 192 KB of operands in flight while needing
+// only 64 B per clock at full MMA rate (a single-CTA 128 x 256 tile needs 96).
+// The pair's accumulator rows live in each CTA's own tensor memory.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over cluster tiles):
-//   warp 0      TMA producer (one elected thread): A and B tiles into a
-//               STAGES-deep shared-memory ring, completion on mbarriers
-//   warp 1      owns the tensor memory; one elected thread issues
-//               tcgen05.mma (128 x 256 x 16 per instruction) and commits
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused elementwise
-//               work, bf16/fp32 stores
+// CTA layout (192 threads, persistent over tiles; both CTAs of the pair):
+//   warp 0      TMA producer (one elected thread): this CTA's A and B halves
+//               into the shared-memory ring; their bytes are counted on the
+//               even CTA's "full" barrier
+//   warp 1      owns the tensor memory (pair allocation); in the even CTA one
+//               elected thread issues the pair MMAs and commits them to both
+//               CTAs' "empty" / "accumulator full" barriers
+//   warps 2..5  epilogue: tcgen05.ld of this CTA's accumulator rows, fused
+//               elementwise work, TMA stores; then they release the
+//               accumulator on the even CTA's "accumulator empty" barrier
 // Two 256-column fp32 accumulators in TMEM let the epilogue of one tile run
 // under the main loop of the next.
 //
-// Every wait is bounded (GemmParams::timeout_ns).  A wait that expires sets a
-// CTA-wide abort flag and a bit of the device error word; every role then
-// leaves its loop, the producer waits (bounded) for its own copies in flight,
-// the MMA issuer waits (bounded) for its own MMAs, and the CTA frees its
-// tensor memory and returns.
+// Every mbarrier wait is bounded (GemmParams::timeout_ns).  A wait that
+// expires sets a CTA-wide abort flag and a bit of the device error word;
+// every role of that CTA then leaves its loop (the peer's waits expire in
+// turn), the even CTA's producer waits (bounded) for copies in flight, the
+// MMA issuer waits (bounded) for its MMAs, and after a final cluster barrier
+// both CTAs free their tensor memory and return.  Before leaving, each
+// producer also waits until every stage it filled has been released, and the
+// MMA issuer until the last accumulators have been released, so no
+// asynchronous arrive can land in a CTA that has exited.
 #pragma once
 
 #include <cuda.h>
@@ -95,6 +103,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Same, with cluster-scope acquire (for barriers the peer CTA arrives on).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_flag,
+                                                     const GemmParams& p, unsigned code) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicOr(p.err, code);
+            return false;
+        }
+    }
+}
+
 // Teardown wait: ignores the abort flag, still bounded.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const GemmParams& p) {
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -130,17 +155,16 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
 // ---- operand loads -----------------------------------------------------------------
 // K-major operand: tensor [rows, K] (inner K), box {BK, ROWS}; one copy.
 // MN-major operand: tensor [K, rows] (inner rows), box {64, BK}; ROWS/64
-// copies, box j landing at dst + j * MN_CHUNK_BYTES.
-// HALF (shared B tile): this CTA loads only half `half` of the rows and
-// multicasts it to both CTAs of the cluster (K-major: box {BK, ROWS/2}).
+// copies, box j landing at dst + j * MN_CHUNK_BYTES.  The bytes complete on
+// `bar`, a shared::cluster address (the even CTA's barrier).
 // PART_ROW: a tile whose rows start past the last token chunk (the second
-// CTA of a cluster tile when T is not a multiple of 256) reads the last
-// chunk's map at out-of-range rows, which TMA fills with zeros; the map index
-// never leaves the encoded maps.
-template <bool MN, int ROWS, bool HALF>
+// CTA of a pair tile when T is not a multiple of 256) reads the last chunk's
+// map at out-of-range rows, which TMA fills with zeros; the map index never
+// leaves the encoded maps.
+template <bool MN, int ROWS>
 __device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, int rows_per_map,
                                              int nmaps, int g, int s, int row0, int kc, int K,
-                                             uint32_t dst, uint32_t bar, int half) {
+                                             uint32_t dst, uint32_t bar) {
     int idx = 0, r = row0, k = s * K + kc;
     if (part == PART_GROUP) {
         idx = g;
@@ -152,26 +176,12 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, 
         r = row0 - idx * rows_per_map;
     }
     const CUtensorMap* m = maps + idx;
-    if constexpr (!HALF) {
-        if constexpr (!MN) {
-            ptx::tma_load_2d(dst, m, k, r, bar);
-        } else {
-#pragma unroll
-            for (int j = 0; j < ROWS / MN_CHUNK; ++j)
-                ptx::tma_load_2d(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
-        }
+    if constexpr (!MN) {
+        ptx::tma_load_2d_pair(dst, m, k, r, bar);
     } else {
-        constexpr int HROWS = ROWS / 2;
-        if constexpr (!MN) {
-            ptx::tma_load_2d_multicast(dst + half * HROWS * 128, m, k, r + half * HROWS, bar, 0x3);
-        } else {
 #pragma unroll
-            for (int jj = 0; jj < HROWS / MN_CHUNK; ++jj) {
-                const int j = half * (HROWS / MN_CHUNK) + jj;
-                ptx::tma_load_2d_multicast(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar,
-                                           0x3);
-            }
-        }
+        for (int j = 0; j < ROWS / MN_CHUNK; ++j)
+            ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
     }
 }
 
@@ -283,11 +293,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     uint8_t* bar_area = epi_area + EPI_STAGE_BYTES;
     const uint32_t epi0 = base + STAGES * STAGE_BYTES;
     const uint32_t bar0 = epi0 + EPI_STAGE_BYTES;
-    const uint32_t bar_full = bar0;                      // [STAGES]
-    const uint32_t bar_empty = bar0 + 8 * STAGES;        // [STAGES]
-    const uint32_t bar_tfull = bar0 + 16 * STAGES;       // [2]
-    const uint32_t bar_tempty = bar_tfull + 16;          // [2]
-    const uint32_t bar_drain = bar_tempty + 16;          // [1]
+    const uint32_t bar_full = bar0;                      // [STAGES] used in the even CTA
+    const uint32_t bar_empty = bar0 + 8 * STAGES;        // [STAGES] both CTAs
+    const uint32_t bar_tfull = bar0 + 16 * STAGES;       // [2] both CTAs
+    const uint32_t bar_tempty = bar_tfull + 16;          // [2] used in the even CTA
+    const uint32_t bar_drain = bar_tempty + 16;          // [1] even CTA
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 16 * STAGES + 40);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 44);
 
@@ -300,11 +310,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, 2);  // released by both CTAs' MMAs
+            ptx::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar_tfull + 8 * a, 1);
-            ptx::mbar_init(bar_tempty + 8 * a, 4 * 32);
+            ptx::mbar_init(bar_tempty + 8 * a, 2 * EPI_WARPS * 32);  // both CTAs' epilogues
         }
         ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -312,10 +322,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         ptx::fence_proxy_async_smem();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
-    // both CTAs' barriers exist before any multicast or remote arrive
+    // both CTAs' barriers and tensor memory exist before anything crosses
     ptx::tc_fence_before();
     __syncwarp();
     ptx::cluster_sync();
@@ -327,7 +337,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer (both CTAs) ----------------
+            const uint32_t even_full = ptx::mapa_shared(bar_full, 0);
             int stage = 0;
             uint32_t phase = 0;
             long long fills = 0;
@@ -336,6 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 int g, m0, n0;
                 decode_tile(p, tile, g, m0, n0);
                 const int a_row = m0 + rank * BM;
+                const int b_row = n0 + rank * B_ROWS;
                 for (int s = 0; ok && s < p.ksegs; ++s) {
                     for (int kb = 0; kb < kblocks; ++kb) {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
@@ -344,15 +356,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             break;
                         }
                         if (!p.stall_producer) {
-                            const uint32_t full = bar_full + 8 * stage;
+                            const uint32_t full = even_full + 8 * stage;
                             const uint32_t sa = base + stage * STAGE_BYTES;
-                            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
-                            load_operand<A_MN, BM, false>(p.a_map, p.a_part, p.a_rows_per_map,
-                                                          p.a_nmaps, g, s, a_row, kb * BK, p.K,
-                                                          sa, full, 0);
-                            load_operand<B_MN, BN, true>(p.b_map, p.b_part, p.b_rows_per_map,
-                                                         p.b_nmaps, g, s, n0, kb * BK, p.K,
-                                                         sa + A_STAGE_BYTES, full, rank);
+                            if (rank == 0)  // counts both CTAs' bytes
+                                ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * STAGE_BYTES);
+                            load_operand<A_MN, BM>(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps,
+                                                   g, s, a_row, kb * BK, p.K, sa, full);
+                            load_operand<B_MN, B_ROWS>(p.b_map, p.b_part, p.b_rows_per_map,
+                                                       p.b_nmaps, g, s, b_row, kb * BK, p.K,
+                                                       sa + A_STAGE_BYTES, full);
                             ++fills;
                         }
                         if (++stage == STAGES) {
@@ -363,10 +375,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             if (ok) {
-                // Producer tail: the peer's MMA releases each stage with an
-                // asynchronous arrive on this CTA's "empty" barrier.  Wait until
-                // every stage filled here has been released by both MMAs, so no
-                // such arrive can land after this CTA has exited.
+                // Producer tail: the even CTA's MMA releases each stage with an
+                // asynchronous arrive on both CTAs' "empty" barriers.  Wait until
+                // every stage filled here has been released, so no such arrive
+                // can land after this CTA has exited.
                 for (int i = 0; i < STAGES; ++i) {
                     if (!wait_drain(bar_empty + 8 * stage, phase ^ 1u, p)) break;
                     if (++stage == STAGES) {
@@ -374,9 +386,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         phase ^= 1u;
                     }
                 }
-            } else {
-                // Wait for the copies into this CTA still in flight (the last
-                // STAGES fills) before the CTA can leave.
+            } else if (rank == 0) {
+                // Wait for the pair's copies still in flight (the last STAGES
+                // fills, counted on this CTA's barriers) before leaving.
                 for (long long f = (fills > STAGES ? fills - STAGES : 0); f < fills; ++f) {
                     const int st = static_cast<int>(f % STAGES);
                     const uint32_t par = static_cast<uint32_t>((f / STAGES) & 1);
@@ -385,9 +397,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (even CTA) ----------------
+            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(CLUSTER_M, BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             int lt = 0;
@@ -395,7 +407,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
-                if (!wait_bounded(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p, ERR_MMA)) {
+                if (!wait_bounded_cluster(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p,
+                                          ERR_MMA)) {
                     ok = false;
                     break;
                 }
@@ -411,21 +424,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     const uint32_t sb = sa + A_STAGE_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        ptx::mma_bf16_ss(d_tmem, operand_desc<A_MN>(sa, k),
-                                         operand_desc<B_MN>(sb, k), IDESC,
-                                         (kk > 0 || k > 0) ? 1u : 0u);
+                        ptx::mma_bf16_pair(d_tmem, operand_desc<A_MN>(sa, k),
+                                           operand_desc<B_MN>(sb, k), IDESC,
+                                           (kk > 0 || k > 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit_multicast(bar_empty + 8 * stage, 0x3);
+                    ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok) ptx::mma_commit(bar_tfull + 8 * acc);
+                if (ok) ptx::mma_commit_pair_multicast(bar_tfull + 8 * acc, 0x3);
             }
             // Every MMA this thread issued must finish before TMEM is freed.
-            ptx::mma_commit(bar_drain);
+            ptx::mma_commit_pair(bar_drain);
             wait_drain(bar_drain, 0, p);
+            // MMA tail: both CTAs' epilogues release the last accumulators with
+            // arrives on this CTA's barriers; wait for them before leaving.
+            if (ok) {
+                for (int j = (lt > 2 ? lt - 2 : 0); j < lt; ++j) {
+                    if (!wait_drain(bar_tempty + 8 * (j & 1),
+                                    static_cast<uint32_t>((j >> 1) & 1), p))
+                        break;
+                }
+            }
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
@@ -433,6 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const int row = quarter * 32 + lane;
         uint8_t* stage_buf = epi_area + (warp - 2) * (2 * EPI_BUF_BYTES);
         const uint32_t stage_u32 = epi0 + (warp - 2) * (2 * EPI_BUF_BYTES);
+        const uint32_t even_tempty = ptx::mapa_shared(bar_tempty, 0);
         int chunk_seq = 0;
         int lt = 0;
         for (int tile = cluster; tile < p.total_tiles; tile += nclusters, ++lt) {
@@ -492,26 +515,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_tempty + 8 * acc);
+            ptx::mbar_arrive_cluster(even_tempty + 8 * acc);
         }
         // every store must have finished before the CTA leaves
         if (lane == 0) ptx::bulk_wait_group<0>();
         __syncwarp();
     }
 
-    // neither CTA leaves while the other may still multicast into it
+    // neither CTA frees its tensor memory or leaves before the pair's MMAs
+    // (which write both CTAs' tensor memory) have drained
     ptx::tc_fence_before();
     __syncwarp();
     ptx::cluster_sync();
     ptx::tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
-// Persistent launch: one 2-CTA cluster per cluster tile, capped at the number
-// of clusters that fit on the GPU at once (queried once per kernel variant).
+// Persistent launch: one CTA pair per tile, capped at the number of pairs
+// that fit on the GPU at once (queried once per kernel variant).
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_clusters(const GemmParams& p, cudaStream_t stream) {
     auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;

@@ -9,16 +9,17 @@
 
 namespace tpmlp {
 
-// Two CTAs of a cluster own vertically adjacent 128 x 256 tiles (a 256 x 256
-// cluster tile) with the same B tile: each loads its own A and one half of B,
-// multicast into both CTAs' shared memory.
-constexpr int BM = 128;       // tile rows per CTA (TMEM lanes)
-constexpr int CLUSTER_M = 2 * BM;  // rows per cluster tile
+// A CTA pair (cluster of 2) computes a CLUSTER_M x BN tile with
+// tcgen05.mma.cta_group::2: each CTA stages its own BM rows of A and its own
+// BN/2 rows of B per K step and holds BM rows x BN columns of the accumulator.
+constexpr int BM = 128;            // tile rows per CTA (TMEM lanes)
+constexpr int CLUSTER_M = 2 * BM;  // tile rows per CTA pair
 constexpr int BN = 256;       // tile columns (TMEM columns per accumulator)
 constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int B_ROWS = BN / 2;     // B rows (output columns) staged per CTA
+constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
@@ -78,8 +79,8 @@ struct GemmParams {
 };
 
 // Launchers, one per (operand majorness, epilogue) variant.  Each launches a
-// persistent grid of 2-CTA clusters (at most one cluster per cluster tile,
-// at most as many clusters as fit on the GPU at once).
+// persistent grid of CTA pairs (at most one pair per tile, at most as many
+// pairs as fit on the GPU at once).
 //   column_fwd : A K-major,  B MN-major, EPI_BIAS_GELU  (Y_i, H_i)
 //   row_fwd    : A K-major,  B MN-major, EPI_BIAS       (Z)
 //   dgrad_h    : A K-major,  B K-major,  EPI_DGELU      (dY_i)
