@@ -84,6 +84,31 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "tensor_transformer_mlp_gemm_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernels have changed since those counters were taken (or for another
+    workload)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_traffic.json")) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash() or workload != "gpt_175b":
+        return None
+    return d.get("dram_bytes_per_launch", {}).get(kernel)
+
+
 def workload_config(w, l2_note):
     return {"workload": f"{w.name}: T={w.tokens} (mb {w.micro_batch} x seq {w.seq}), "
                         f"h={w.hidden}, f={w.ffn}, t={w.t}, seq_chunks={w.seq_chunks}",
@@ -355,7 +380,8 @@ def run_ours(args, torch):
         achieved = 2.0 * T * h * f / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"], "traffic": None,
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "traffic": measured_traffic(dom, w.name),
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long "
                                f"step); frac of burst {peaks['bf16_tflops']}: "
                                f"{achieved / peaks['bf16_tflops']:.3f}",
