@@ -147,6 +147,15 @@ const char* tpmlp_status_string(tpmlp_status s);
  * usable. */
 tpmlp_status tpmlp_sync_check(void* stream);
 
+/* Tail split of the GEMMs.  When a GEMM's output tiles do not fill the last
+ * wave of CTA pairs, the K ranges of the leftover tiles are split across the
+ * pairs that would otherwise idle; each part writes an fp32 partial tile into
+ * the workspace and the last part to finish sums them in a fixed order (the
+ * result stays bitwise reproducible) before the fused epilogue.  This is done
+ * only for tiles at least `kblocks` 64-deep K steps long (default 128); 0
+ * turns it off.  Affects launches enqueued after the call. */
+tpmlp_status tpmlp_set_split_min_kblocks(int kblocks);
+
 /* Upper bound, in nanoseconds, on any single wait inside a kernel of this
  * library (default 2e9).  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);

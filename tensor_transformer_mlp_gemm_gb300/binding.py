@@ -34,7 +34,7 @@ EXPORTED = (
     "tpmlp_workspace_bytes", "tpmlp_workspace_layout", "tpmlp_forward", "tpmlp_backward",
     "tpmlp_status_string", "tpmlp_sync_check", "tpmlp_set_wait_timeout_ns",
     "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
-    "tpmlp_kernel_name", "tpmlp_column_sums_noalloc",
+    "tpmlp_kernel_name", "tpmlp_column_sums_noalloc", "tpmlp_set_split_min_kblocks",
 )
 
 
@@ -66,6 +66,8 @@ _lib.tpmlp_status_string.restype = ctypes.c_char_p
 _lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 _lib.tpmlp_sync_check.restype = ctypes.c_int
 _lib.tpmlp_sync_check.argtypes = [_vp]
+_lib.tpmlp_set_split_min_kblocks.restype = ctypes.c_int
+_lib.tpmlp_set_split_min_kblocks.argtypes = [ctypes.c_int]
 _lib.tpmlp_set_wait_timeout_ns.restype = ctypes.c_int
 _lib.tpmlp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.tpmlp_selftest_stalled_gemm.restype = ctypes.c_int
@@ -155,6 +157,10 @@ def tpmlp_backward(dims, dZ, X, A_shards, B_shards, workspace, dX, dA_shards, db
 def tpmlp_sync_check(stream=None) -> int:
     """Returns the status (does not raise), so callers can test for TIMEOUT."""
     return int(_lib.tpmlp_sync_check(_stream(stream)))
+
+
+def tpmlp_set_split_min_kblocks(kblocks: int) -> None:
+    _check(_lib.tpmlp_set_split_min_kblocks(int(kblocks)), "tpmlp_set_split_min_kblocks")
 
 
 def tpmlp_set_wait_timeout_ns(ns: int) -> None:

@@ -152,6 +152,41 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     m0 = mt * CLUSTER_M;
 }
 
+// ---- work items -------------------------------------------------------------------
+// Pair c first takes split unit c (if c < units): K steps [kbeg, kend) of
+// leftover tile dp_tiles + c / splits; then whole tiles c, c + P, ... below
+// dp_tiles.  Every role of both CTAs walks the same sequence.
+struct WorkItem {
+    int tile;
+    int kbeg, kend;
+    int unit;  // split unit index, or -1 for a whole tile
+};
+
+__device__ __forceinline__ bool work_item(const GemmParams& p, int c, int P, int j, int nk,
+                                          WorkItem& it) {
+    const int has_split = c < p.units ? 1 : 0;
+    if (has_split && j == 0) {
+        const int sidx = c % p.splits;
+        it.unit = c;
+        it.tile = p.dp_tiles + c / p.splits;
+        it.kbeg = sidx * nk / p.splits;
+        it.kend = (sidx + 1) * nk / p.splits;
+        return true;
+    }
+    const int tile = c + (j - has_split) * P;
+    if (tile >= p.dp_tiles) return false;
+    it.tile = tile;
+    it.kbeg = 0;
+    it.kend = nk;
+    it.unit = -1;
+    return true;
+}
+
+// Named barrier among the four epilogue warps of a CTA.
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory");
+}
+
 // ---- operand loads -----------------------------------------------------------------
 // K-major operand: tensor [rows, K] (inner K), box {BK, ROWS}; one copy.
 // MN-major operand: tensor [K, rows] (inner rows), box {64, BK}; ROWS/64
@@ -300,6 +335,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t bar_drain = bar_tempty + 16;          // [1] even CTA
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 16 * STAGES + 40);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 44);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 48);
+    volatile int* epi_fail = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 52);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -318,6 +355,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         ptx::mbar_init(bar_drain, 1);
         *abort_flag = 0;
+        *last_flag = 0;
+        *epi_fail = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -343,13 +382,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             uint32_t phase = 0;
             long long fills = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters) {
+            WorkItem it;
+            for (int j = 0; ok && work_item(p, cluster, nclusters, j, nk, it); ++j) {
                 int g, m0, n0;
-                decode_tile(p, tile, g, m0, n0);
+                decode_tile(p, it.tile, g, m0, n0);
                 const int a_row = m0 + rank * BM;
                 const int b_row = n0 + rank * B_ROWS;
-                for (int s = 0; ok && s < p.ksegs; ++s) {
-                    for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kk = it.kbeg; kk < it.kend; ++kk) {
+                    const int s = kk / kblocks;
+                    const int kb = kk - s * kblocks;
+                    {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
                                           ERR_PRODUCER)) {
                             ok = false;
@@ -404,7 +446,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             uint32_t phase = 0;
             int lt = 0;
             bool ok = true;
-            for (int tile = cluster; ok && tile < p.total_tiles; tile += nclusters, ++lt) {
+            WorkItem it;
+            for (int j = 0; ok && work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
                 const int acc = lt & 1;
                 const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
                 if (!wait_bounded_cluster(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p,
@@ -414,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kk = 0; kk < nk; ++kk) {
+                for (int kk = it.kbeg; kk < it.kend; ++kk) {
                     if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p, ERR_MMA)) {
                         ok = false;
                         break;
@@ -426,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     for (int k = 0; k < BK / 16; ++k) {
                         ptx::mma_bf16_pair(d_tmem, operand_desc<A_MN>(sa, k),
                                            operand_desc<B_MN>(sb, k), IDESC,
-                                           (kk > 0 || k > 0) ? 1u : 0u);
+                                           (kk > it.kbeg || k > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
                     if (++stage == STAGES) {
@@ -457,16 +500,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t stage_u32 = epi0 + (warp - 2) * (2 * EPI_BUF_BYTES);
         const uint32_t even_tempty = ptx::mapa_shared(bar_tempty, 0);
         int chunk_seq = 0;
+
+        // Stage 32 values per lane as this warp's 32 x 32 box and store it
+        // through `map` at (x, y) (and the second output for EPI_BIAS_GELU).
+        auto store_box = [&](const CUtensorMap* map, const CUtensorMap* map2, int x, int y,
+                             const float (&v)[32], const float (&v2)[32], bool f32) {
+            const int b = chunk_seq & 1;
+            ++chunk_seq;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+            uint8_t* buf = stage_buf + b * EPI_BUF_BYTES;
+            if (f32) {
+                stage_row_f32(buf, lane, v);
+            } else {
+                stage_row_bf16(buf, lane, v);
+                if (map2) stage_row_bf16(buf + 2048, lane, v2);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t sb = stage_u32 + b * EPI_BUF_BYTES;
+                ptx::tma_store_2d(map, sb, x, y);
+                if (!f32 && map2) ptx::tma_store_2d(map2, sb + 2048, x, y);
+                ptx::bulk_commit_group();
+            }
+        };
+
         int lt = 0;
-        for (int tile = cluster; tile < p.total_tiles; tile += nclusters, ++lt) {
+        WorkItem it;
+        for (int j = 0; work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
             int g, mp, n0;
-            decode_tile(p, tile, g, mp, n0);
+            decode_tile(p, it.tile, g, mp, n0);
             const int m0 = mp + rank * BM;  // this CTA's first row
             const int acc = lt & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
             const bool ok = wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag, p,
                                          ERR_EPILOGUE);
-            if (__any_sync(0xffffffffu, !ok)) break;
+            // all four epilogue warps give up together (they share named barriers)
+            if (!ok) *epi_fail = 1;
+            epilogue_bar();
+            if (*epi_fail) break;
             __syncwarp();
             ptx::tc_fence_after();
             // output map and row coordinate of this warp's 32 rows
@@ -480,42 +553,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const long long in_row = static_cast<long long>(y0) + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            const CUtensorMap* out1 = &p.out_map[part];
+            const CUtensorMap* out2 = EPI == EPI_BIAS_GELU ? &p.out_map[MAX_MAPS + part] : nullptr;
+            constexpr bool OUT_F32 = EPI == EPI_F32;
+
+            if (it.unit < 0) {
+                // whole tile: fused epilogue straight from the accumulator
+#pragma unroll 1
+                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
+                    ptx::tmem_ld_wait();
+                    const int n = n0 + c * EPI_CHUNK;
+                    if (n >= p.N || m0 >= p.M) continue;  // outside the tensor (warp-uniform)
+                    float x[32], x2[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                    store_box(out1, out2, n, y0, x, x2, OUT_F32);
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive_cluster(even_tempty + 8 * acc);
+                continue;
+            }
+
+            // split unit: store this unit's raw partial rows, then count it
+            const int prow = (it.unit * 2 + rank) * BM + quarter * 32;
 #pragma unroll 1
             for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                 ptx::tmem_ld_wait();
                 const int n = n0 + c * EPI_CHUNK;
-                if (n >= p.N || m0 >= p.M) continue;  // chunk outside the tensor (warp-uniform)
-                float x[32], x2[32];
+                if (n >= p.N || m0 >= p.M) continue;
+                float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-                epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
-                // staging buffer of this chunk: free once the store issued two
-                // chunks ago has finished reading it
-                const int b = chunk_seq & 1;
-                ++chunk_seq;
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
-                __syncwarp();
-                uint8_t* buf = stage_buf + b * EPI_BUF_BYTES;
-                if constexpr (EPI == EPI_F32) {
-                    stage_row_f32(buf, lane, x);
-                } else {
-                    stage_row_bf16(buf, lane, x);
-                    if constexpr (EPI == EPI_BIAS_GELU) stage_row_bf16(buf + 2048, lane, x2);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t sb = stage_u32 + b * EPI_BUF_BYTES;
-                    ptx::tma_store_2d(&p.out_map[part], sb, n, y0);
-                    if constexpr (EPI == EPI_BIAS_GELU)
-                        ptx::tma_store_2d(&p.out_map[MAX_MAPS + part], sb + 2048, n, y0);
-                    ptx::bulk_commit_group();
-                }
+                for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
+                store_box(&p.part_map, nullptr, c * EPI_CHUNK, prow, x, x, true);
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive_cluster(even_tempty + 8 * acc);
+            // the partial is complete and visible before it is counted
+            if (lane == 0) {
+                ptx::bulk_wait_group<0>();
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
+            epilogue_bar();
+            const int slot = (it.tile - p.dp_tiles) * 2 + rank;
+            if (warp == 2 && lane == 0) {
+                __threadfence();
+                const int before = atomicAdd(&p.counters[slot], 1);
+                *last_flag = (before == p.splits - 1) ? 1 : 0;
+            }
+            epilogue_bar();
+            if (*last_flag) {
+                // last unit of this tile: sum all partials in unit order, then
+                // the fused epilogue
+                __threadfence();
+                const int u0 = (it.tile - p.dp_tiles) * p.splits;
+#pragma unroll 1
+                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                    const int n = n0 + c * EPI_CHUNK;
+                    if (n >= p.N || m0 >= p.M) continue;
+                    float x[32], x2[32];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) x[q] = 0.f;
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        const long long r = static_cast<long long>((u0 + sp) * 2 + rank) * BM + row;
+                        const float4* src =
+                            reinterpret_cast<const float4*>(p.partial + r * BN + c * EPI_CHUNK);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 f = __ldcg(src + q);
+                            x[4 * q] += f.x;
+                            x[4 * q + 1] += f.y;
+                            x[4 * q + 2] += f.z;
+                            x[4 * q + 3] += f.w;
+                        }
+                    }
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                    store_box(out1, out2, n, y0, x, x2, OUT_F32);
+                }
+                if (warp == 2 && lane == 0) p.counters[slot] = 0;  // ready for the next launch
+            }
         }
         // every store must have finished before the CTA leaves
         if (lane == 0) ptx::bulk_wait_group<0>();
@@ -537,7 +658,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 // Persistent launch: one CTA pair per tile, capped at the number of pairs
 // that fit on the GPU at once (queried once per kernel variant).
 template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_clusters(const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
+    GemmParams p = p_in;
     auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;
     static int max_clusters = 0;
     if (max_clusters == 0) {
@@ -561,7 +683,31 @@ cudaError_t launch_clusters(const GemmParams& p, cudaStream_t stream) {
         if (n < 1) return cudaErrorInvalidConfiguration;
         max_clusters = n;
     }
-    const int clusters = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+    // Tail split: the tiles of an incomplete last wave of pairs get their K
+    // range split across the pairs that would otherwise idle.
+    const int P = max_clusters;
+    const int nk = ((p.K + BK - 1) / BK) * p.ksegs;
+    const int full = p.total_tiles / P;
+    const int left = p.total_tiles % P;
+    p.dp_tiles = p.total_tiles;
+    p.units = 0;
+    p.splits = 1;
+    if (p.counters && p.split_min_kblocks > 0 && nk >= p.split_min_kblocks && left > 0) {
+        int splits = P / left;
+        if (splits > MAX_SPLITS) splits = MAX_SPLITS;
+        if (splits > nk) splits = nk;
+        if (splits >= 2 && left * splits <= MAX_SPLIT_UNITS) {
+            p.splits = splits;
+            p.units = left * splits;
+            p.dp_tiles = p.total_tiles - left;
+        }
+    }
+    int clusters = p.total_tiles < P ? p.total_tiles : P;
+    if (p.units > 0) {
+        clusters = full > 0 ? P : p.units;
+        cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int) * 2 * left, stream);
+        if (e != cudaSuccess) return e;
+    }
     kern<<<2 * clusters, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
 }

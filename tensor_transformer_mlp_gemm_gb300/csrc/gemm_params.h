@@ -30,6 +30,13 @@ constexpr int EPI_BUF_BYTES = 4096;           // one staged 32 x 32 chunk (fp32,
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // double-buffered per warp
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES;
 constexpr int MAX_MAPS = 8;
+// Tail split: when the tiles do not fill the last wave of pairs, the leftover
+// tiles' K ranges are split across the idle pairs.  Each split unit writes an
+// fp32 partial tile; the last unit of a tile to finish sums them in a fixed
+// order and runs the epilogue.
+constexpr int MAX_SPLIT_UNITS = 128;       // partial tiles the workspace holds
+constexpr int MAX_SPLITS = 8;              // K splits per leftover tile
+constexpr int DEFAULT_SPLIT_MIN_KBLOCKS = 128;  // split only tiles this deep in K
 constexpr int MN_CHUNK = 64;                      // elements per 128-byte row
 constexpr int MN_CHUNK_BYTES = MN_CHUNK * BK * 2;  // one MN-major box [BK][64]
 
@@ -62,6 +69,14 @@ struct GemmParams {
     int a_part, b_part;
     int a_rows_per_map, b_rows_per_map;
     int a_nmaps, b_nmaps;   // encoded maps; PART_ROW indices are clamped to them
+    // tail split (set by the launcher; units = 0 means every tile is whole)
+    int dp_tiles;           // tiles computed whole, in schedule order 0..dp_tiles-1
+    int splits;             // K splits per leftover tile
+    int units;              // leftover tiles x splits
+    int split_min_kblocks;  // split only when a tile has at least this many K steps
+    CUtensorMap part_map;   // fp32 [MAX_SPLIT_UNITS * CLUSTER_M, BN] partial tiles
+    const float* partial;   // same buffer, for the summing loads
+    int* counters;          // [MAX_SPLIT_UNITS][2] arrivals per leftover tile and CTA
     int mtiles, ntiles, total_tiles, band;  // cluster tiles of CLUSTER_M x BN
     // epilogue: TMA store maps (box 32 x 32, 128-byte swizzle for fp32,
     // 64-byte swizzle for bf16) and the saved pre-activation for EPI_DGELU

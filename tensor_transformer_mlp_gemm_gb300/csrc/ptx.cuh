@@ -149,6 +149,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
         : "memory");
 }
 
+// Orders this thread's completed async-proxy global writes (TMA stores)
+// before its later generic-proxy operations (a fence and a flag write).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

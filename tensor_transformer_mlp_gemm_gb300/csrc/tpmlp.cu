@@ -57,6 +57,7 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = 2000000000ULL;
+int g_split_min_kblocks = DEFAULT_SPLIT_MIN_KBLOCKS;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -171,7 +172,7 @@ bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, b
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t y, h, dy, part1, part2, total;
+    size_t y, h, dy, part1, part2, split_part, split_cnt, total;
 };
 
 Layout layout_of(const tpmlp_dims& d) {
@@ -182,7 +183,9 @@ Layout layout_of(const tpmlp_dims& d) {
     L.dy = 2 * act;
     L.part1 = 3 * act;
     L.part2 = L.part1 + align256(colsum_scratch_bytes(d.ffn));
-    L.total = L.part2 + align256(colsum_scratch_bytes(d.hidden));
+    L.split_part = L.part2 + align256(colsum_scratch_bytes(d.hidden));
+    L.split_cnt = L.split_part + align256(static_cast<size_t>(MAX_SPLIT_UNITS) * CLUSTER_M * BN * 4);
+    L.total = L.split_cnt + align256(static_cast<size_t>(MAX_SPLIT_UNITS) * 2 * sizeof(int));
     return L;
 }
 
@@ -253,6 +256,23 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
 }
 
+// Workspace buffers of the tail split (see gemm_params.h).
+bool attach_split(GemmParams& p, uint8_t* ws, const Layout& L) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(BN),
+                          static_cast<cuuint64_t>(MAX_SPLIT_UNITS) * CLUSTER_M};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(BN) * 4};
+    cuuint32_t box[2] = {EPI_CHUNK, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + L.split_part, dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    p.partial = reinterpret_cast<const float*>(ws + L.split_part);
+    p.counters = reinterpret_cast<int*>(ws + L.split_cnt);
+    p.split_min_kblocks = g_split_min_kblocks;
+    return true;
+}
+
 struct Shapes {
     int T, h, f, t, fi, chunks, Tc;
 };
@@ -302,6 +322,13 @@ TPMLP_API tpmlp_status tpmlp_workspace_layout(const tpmlp_dims* dims, size_t* y_
     if (y_offset) *y_offset = L.y;
     if (h_offset) *h_offset = L.h;
     if (dy_offset) *dy_offset = L.dy;
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_set_split_min_kblocks(int kblocks) {
+    if (kblocks < 0) return TPMLP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_split_min_kblocks = kblocks;
     return TPMLP_OK;
 }
 
@@ -360,6 +387,7 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.out_rows_per_part = 0;
         p.bias = b1;
         p.bias_group_stride = s.fi;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_COLUMN_FWD, 1, st,
                          [&] { return launch_column_fwd(p, st); }));
     }
@@ -382,6 +410,7 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
         p.bias = b2;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
                          [&] { return launch_row_fwd(p, st); }));
     }
@@ -448,6 +477,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
         p.ld_in = s.fi;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
                          [&] { return launch_dgrad_h(p, st); }));
     }
@@ -469,6 +499,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
             if (!encode_out(&p.out_map[j], dX[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
                          [&] { return launch_dgrad_x(p, st); }));
     }
@@ -491,6 +522,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
                 return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
                          [&] { return launch_wgrad(p, st); }));
     }
@@ -513,6 +545,7 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
                 return TPMLP_ERR_UNSUPPORTED;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
+        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
                          [&] { return launch_wgrad(p, st); }));
     }

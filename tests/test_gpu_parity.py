@@ -163,6 +163,38 @@ def test_deterministic_rerun():
     assert torch.equal(a.db1, b.db1) and torch.equal(a.db2, b.db2)
 
 
+@pytest.fixture
+def forced_tail_split():
+    """Split the leftover tiles of every GEMM, however short its K range, so
+    the partial-tile path runs at sizes the full oracle covers."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    binding.tpmlp_set_split_min_kblocks(1)
+    yield
+    binding.tpmlp_set_split_min_kblocks(128)
+
+
+@pytest.mark.parametrize("T,h,f,t,chunks", [
+    (128, 256, 1024, 2, 1),    # the tiny workload: every GEMM's tiles split
+    (333, 264, 1032, 3, 1),    # ragged tails inside split tiles
+    (512, 256, 1024, 4, 4),    # sequence-parallel chunks
+])
+def test_tail_split_full(forced_tail_split, T, h, f, t, chunks):
+    _run_full(custom(T, h, f, t, sigma_w=0.05, seq_chunks=chunks), seed=12)
+
+
+def test_tail_split_deterministic(forced_tail_split):
+    w = custom(333, 264, 1032, 3)
+    inputs = make_inputs(w, 13)
+    a, b = _block(w, inputs), _block(w, inputs)
+    a.step()
+    b.step()
+    torch.cuda.synchronize()
+    _assert_bitwise(a.Z, b.Z, "Z")
+    _assert_bitwise(a.dX, b.dX, "dX")
+    _assert_bitwise(a.dA, b.dA, "dA")
+    _assert_bitwise(a.dB, b.dB, "dB")
+
+
 def test_stalled_gemm_reports_timeout_and_context_survives():
     from tensor_transformer_mlp_gemm_gb300 import binding
     dev = torch.device("cuda:0")
