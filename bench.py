@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--ffn", type=int, help="override f")
     ap.add_argument("--t", type=int, help="override the shard count")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--split-min-kblocks", type=int, default=None,
+                    help="tail-split depth threshold of the GEMMs (0 = off; library default 128)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -328,6 +330,8 @@ def run_ours(args, torch):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.split_min_kblocks is not None:
+        binding.tpmlp_set_split_min_kblocks(args.split_min_kblocks)
     w = pick_workload(args)
     inputs = make_inputs(w, 0)
     blk = DeviceBlock(w, inputs, device=dev)
