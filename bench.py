@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--ffn", type=int, help="override f")
     ap.add_argument("--t", type=int, help="override the shard count")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--recompute", action="store_true",
+                    help="selective recompute: keep only Y between passes, rebuild H in backward")
     ap.add_argument("--split-min-kblocks", type=int, default=None,
                     help="tail-split depth threshold of the GEMMs (0 = off; library default 128)")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -334,7 +336,7 @@ def run_ours(args, torch):
         binding.tpmlp_set_split_min_kblocks(args.split_min_kblocks)
     w = pick_workload(args)
     inputs = make_inputs(w, 0)
-    blk = DeviceBlock(w, inputs, device=dev)
+    blk = DeviceBlock(w, inputs, device=dev, recompute=args.recompute)
     stream = torch.cuda.current_stream(dev)
     T, h, f = w.tokens, w.hidden, w.ffn
     flops_step = 12.0 * T * h * f
@@ -438,11 +440,21 @@ def run_ours(args, torch):
                         d.copy_(h, non_blocking=True)
                     ev["in_ready"][b].record(copy_stream)
                 stream.wait_event(ev["in_ready"][b])
-                binding.tpmlp_forward(blk.dims, B["X"], blk.A, blk.b1, blk.B, blk.b2, w.t,
-                                      B["Z"], blk.ws, stream)
+                if args.recompute:
+                    binding.tpmlp_forward_recompute(blk.dims, B["X"], blk.A, blk.b1, blk.B,
+                                                    blk.b2, w.t, B["Z"], blk.saved_y,
+                                                    blk.scratch, stream)
+                else:
+                    binding.tpmlp_forward(blk.dims, B["X"], blk.A, blk.b1, blk.B, blk.b2, w.t,
+                                          B["Z"], blk.ws, stream)
                 ev["fwd_done"][b].record(stream)
-                binding.tpmlp_backward(blk.dims, B["dZ"], B["X"], blk.A, blk.B, blk.ws, B["dX"],
-                                       blk.dA, blk.db1, blk.dB, blk.db2, stream)
+                if args.recompute:
+                    binding.tpmlp_backward_recompute(blk.dims, B["dZ"], B["X"], blk.A, blk.B,
+                                                     blk.saved_y, blk.scratch, B["dX"], blk.dA,
+                                                     blk.db1, blk.dB, blk.db2, stream)
+                else:
+                    binding.tpmlp_backward(blk.dims, B["dZ"], B["X"], blk.A, blk.B, blk.ws,
+                                           B["dX"], blk.dA, blk.db1, blk.dB, blk.db2, stream)
                 ev["bwd_done"][b].record(stream)
                 with torch.cuda.stream(copy_stream):
                     copy_stream.wait_event(ev["fwd_done"][b])
@@ -486,7 +498,8 @@ def run_ours(args, torch):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": workload_config(w, l2_note),
+                "config": {**workload_config(w, l2_note),
+                           "activation_recompute": bool(args.recompute)},
                 "tokens_per_s": tokens_s,
                 "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
                                      "sustained": value / world / peaks["bf16_tflops_sustained"],

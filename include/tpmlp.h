@@ -136,6 +136,38 @@ tpmlp_status tpmlp_backward(const tpmlp_dims* dims,
                             void* const* dB_shards, void* db2,
                             void* stream);
 
+/* Selective recompute ("融合优化技术" and "高级特性 / 选择性激活重计算" on
+ * "Megatron-LM：NVIDIA 的大规模并行训练方案": keep part of the activations,
+ * recompute the rest in the backward pass).  Same block, same results for
+ * Z, dX, dA, db1 and db2 (bitwise); dB is computed from H = GeLU(Y) rebuilt
+ * from the saved bf16 Y, so it may differ from tpmlp_backward's in the last
+ * bits.  Only Y (T x f bf16) is kept between the forward and the backward
+ * pass ("saved", per layer); H, dY and the partial sums live in "scratch",
+ * which holds nothing between calls and can be shared by all layers that run
+ * on one stream.  The dH GEMM's epilogue rebuilds H from Y as it computes dY.
+ *   saved   >= *saved_bytes device bytes: written by the forward, read by the backward
+ *   scratch >= *scratch_bytes device bytes: used during either call only
+ * Other arguments, layouts and errors as tpmlp_forward / tpmlp_backward. */
+tpmlp_status tpmlp_recompute_workspace_bytes(const tpmlp_dims* dims, size_t* saved_bytes,
+                                             size_t* scratch_bytes);
+tpmlp_status tpmlp_forward_recompute(const tpmlp_dims* dims,
+                                     const void* const* X,
+                                     const void* const* A_shards, const void* b1,
+                                     const void* const* B_shards, const void* b2,
+                                     int t,
+                                     void* const* Z,
+                                     void* saved, void* scratch, void* stream);
+tpmlp_status tpmlp_backward_recompute(const tpmlp_dims* dims,
+                                      const void* const* dZ,
+                                      const void* const* X,
+                                      const void* const* A_shards,
+                                      const void* const* B_shards,
+                                      void* saved, void* scratch,
+                                      void* const* dX,
+                                      void* const* dA_shards, void* db1,
+                                      void* const* dB_shards, void* db2,
+                                      void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* tpmlp_status_string(tpmlp_status s);
 

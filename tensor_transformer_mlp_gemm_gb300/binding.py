@@ -35,6 +35,7 @@ EXPORTED = (
     "tpmlp_status_string", "tpmlp_sync_check", "tpmlp_set_wait_timeout_ns",
     "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
     "tpmlp_kernel_name", "tpmlp_column_sums_noalloc", "tpmlp_set_split_min_kblocks",
+    "tpmlp_recompute_workspace_bytes", "tpmlp_forward_recompute", "tpmlp_backward_recompute",
 )
 
 
@@ -62,6 +63,14 @@ _lib.tpmlp_forward.restype = ctypes.c_int
 _lib.tpmlp_forward.argtypes = [_dims_p, _vpp, _vpp, _vp, _vpp, _vp, ctypes.c_int, _vpp, _vp, _vp]
 _lib.tpmlp_backward.restype = ctypes.c_int
 _lib.tpmlp_backward.argtypes = [_dims_p, _vpp, _vpp, _vpp, _vpp, _vp, _vpp, _vpp, _vp, _vpp, _vp, _vp]
+_lib.tpmlp_recompute_workspace_bytes.restype = ctypes.c_int
+_lib.tpmlp_recompute_workspace_bytes.argtypes = [_dims_p, _sz_p, _sz_p]
+_lib.tpmlp_forward_recompute.restype = ctypes.c_int
+_lib.tpmlp_forward_recompute.argtypes = [_dims_p, _vpp, _vpp, _vp, _vpp, _vp, ctypes.c_int, _vpp,
+                                         _vp, _vp, _vp]
+_lib.tpmlp_backward_recompute.restype = ctypes.c_int
+_lib.tpmlp_backward_recompute.argtypes = [_dims_p, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _vpp, _vpp,
+                                          _vp, _vpp, _vp, _vp]
 _lib.tpmlp_status_string.restype = ctypes.c_char_p
 _lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 _lib.tpmlp_sync_check.restype = ctypes.c_int
@@ -152,6 +161,31 @@ def tpmlp_backward(dims, dZ, X, A_shards, B_shards, workspace, dX, dA_shards, db
                                _arr(B_shards), _ptr(workspace), _arr(dX), _arr(dA_shards),
                                _ptr(db1), _arr(dB_shards), _ptr(db2), _stream(stream)),
            "tpmlp_backward")
+
+
+def tpmlp_recompute_workspace_bytes(dims: tpmlp_dims) -> tuple[int, int]:
+    """(saved bytes kept from forward to backward, scratch bytes used during a call)."""
+    sv, sc = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.tpmlp_recompute_workspace_bytes(ctypes.byref(dims), ctypes.byref(sv),
+                                                ctypes.byref(sc)), "tpmlp_recompute_workspace_bytes")
+    return sv.value, sc.value
+
+
+def tpmlp_forward_recompute(dims, X, A_shards, b1, B_shards, b2, t, Z, saved, scratch,
+                            stream=None) -> None:
+    _check(_lib.tpmlp_forward_recompute(ctypes.byref(dims), _arr(X), _arr(A_shards), _ptr(b1),
+                                        _arr(B_shards), _ptr(b2), int(t), _arr(Z), _ptr(saved),
+                                        _ptr(scratch), _stream(stream)),
+           "tpmlp_forward_recompute")
+
+
+def tpmlp_backward_recompute(dims, dZ, X, A_shards, B_shards, saved, scratch, dX, dA_shards,
+                             db1, dB_shards, db2, stream=None) -> None:
+    _check(_lib.tpmlp_backward_recompute(ctypes.byref(dims), _arr(dZ), _arr(X), _arr(A_shards),
+                                         _arr(B_shards), _ptr(saved), _ptr(scratch), _arr(dX),
+                                         _arr(dA_shards), _ptr(db1), _arr(dB_shards), _ptr(db2),
+                                         _stream(stream)),
+           "tpmlp_backward_recompute")
 
 
 def tpmlp_sync_check(stream=None) -> int:

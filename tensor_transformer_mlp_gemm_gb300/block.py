@@ -14,7 +14,11 @@ from .inputs import Workload, column_shards, row_shards, seq_chunks
 
 
 class DeviceBlock:
-    def __init__(self, w: Workload, inputs: dict, device="cuda:0"):
+    def __init__(self, w: Workload, inputs: dict, device="cuda:0", recompute: bool = False,
+                 scratch: torch.Tensor | None = None):
+        """recompute=True runs the selective-recompute calls: only Y is kept
+        between forward and backward (self.saved_y); H and dY live in a
+        scratch buffer that several blocks on one stream may share."""
         dev = torch.device(device)
         self.w = w
         self.device = dev
@@ -34,28 +38,49 @@ class DeviceBlock:
         self.dB = [torch.empty(fi, h, dtype=torch.float32, device=dev) for _ in range(t)]
         self.db1 = torch.empty(f, dtype=torch.float32, device=dev)
         self.db2 = torch.empty(h, dtype=torch.float32, device=dev)
-        self.ws = torch.empty(max(binding.tpmlp_workspace_bytes(self.dims), 256),
-                              dtype=torch.uint8, device=dev)
+        self.recompute = recompute
+        if recompute:
+            sv, sc = binding.tpmlp_recompute_workspace_bytes(self.dims)
+            self.saved_y = torch.empty(max(sv, 256), dtype=torch.uint8, device=dev)
+            self.scratch = scratch if scratch is not None else torch.empty(
+                max(sc, 256), dtype=torch.uint8, device=dev)
+            self.ws = None
+        else:
+            self.ws = torch.empty(max(binding.tpmlp_workspace_bytes(self.dims), 256),
+                                  dtype=torch.uint8, device=dev)
 
     def forward(self, stream=None) -> None:
-        binding.tpmlp_forward(self.dims, self.X, self.A, self.b1, self.B, self.b2, self.w.t,
-                              self.Z, self.ws, stream)
+        if self.recompute:
+            binding.tpmlp_forward_recompute(self.dims, self.X, self.A, self.b1, self.B, self.b2,
+                                            self.w.t, self.Z, self.saved_y, self.scratch, stream)
+        else:
+            binding.tpmlp_forward(self.dims, self.X, self.A, self.b1, self.B, self.b2, self.w.t,
+                                  self.Z, self.ws, stream)
 
     def backward(self, stream=None) -> None:
-        binding.tpmlp_backward(self.dims, self.dZ, self.X, self.A, self.B, self.ws, self.dX,
-                               self.dA, self.db1, self.dB, self.db2, stream)
+        if self.recompute:
+            binding.tpmlp_backward_recompute(self.dims, self.dZ, self.X, self.A, self.B,
+                                             self.saved_y, self.scratch, self.dX, self.dA,
+                                             self.db1, self.dB, self.db2, stream)
+        else:
+            binding.tpmlp_backward(self.dims, self.dZ, self.X, self.A, self.B, self.ws, self.dX,
+                                   self.dA, self.db1, self.dB, self.db2, stream)
 
     def step(self, stream=None) -> None:
         self.forward(stream)
         self.backward(stream)
 
     def saved(self) -> dict:
-        """Views of the workspace's Y, H, dY as lists of t [T, fi] bf16 tensors."""
+        """Views of Y, H, dY as lists of t [T, fi] bf16 tensors (with recompute:
+        Y in the saved buffer, H and dY in the scratch buffer)."""
         T, fi, t = self.w.tokens, self.w.ffn // self.w.t, self.w.t
         y, h, dy = binding.tpmlp_workspace_layout(self.dims)
         n = T * fi * 2
 
-        def view(off):
-            return [self.ws[off + i * n: off + (i + 1) * n].view(torch.bfloat16).view(T, fi)
+        def view(buf, off):
+            return [buf[off + i * n: off + (i + 1) * n].view(torch.bfloat16).view(T, fi)
                     for i in range(t)]
-        return {"Y": view(y), "H": view(h), "dY": view(dy)}
+        if self.recompute:
+            return {"Y": view(self.saved_y, 0), "H": view(self.scratch, 0),
+                    "dY": view(self.scratch, dy - h)}
+        return {"Y": view(self.ws, y), "H": view(self.ws, h), "dY": view(self.ws, dy)}

@@ -299,7 +299,7 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
             for (int j = 0; j < 32; ++j) x2[j] = gelu_f(x[j]);
         }
     }
-    if constexpr (EPI == EPI_DGELU) {
+    if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
         if (m < p.M) {
             const __nv_bfloat16* y =
                 static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
@@ -309,7 +309,10 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
                     float yf[8];
                     unpack_bf16x8(*reinterpret_cast<const uint4*>(y + 8 * q), yf);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) x[8 * q + j] *= gelu_grad_f(yf[j]);
+                    for (int j = 0; j < 8; ++j) {
+                        x[8 * q + j] *= gelu_grad_f(yf[j]);
+                        if constexpr (EPI == EPI_DGELU_H) x2[8 * q + j] = gelu_f(yf[j]);
+                    }
                 }
             }
         }
@@ -554,7 +557,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             const CUtensorMap* out1 = &p.out_map[part];
-            const CUtensorMap* out2 = EPI == EPI_BIAS_GELU ? &p.out_map[MAX_MAPS + part] : nullptr;
+            const CUtensorMap* out2 = (EPI == EPI_BIAS_GELU || EPI == EPI_DGELU_H)
+                                          ? &p.out_map[MAX_MAPS + part]
+                                          : nullptr;
             constexpr bool OUT_F32 = EPI == EPI_F32;
 
             if (it.unit < 0) {

@@ -7,5 +7,8 @@
 
 namespace tpmlp {
 TPMLP_GEMM_LAUNCHER(launch_dgrad_h, false, false, EPI_DGELU)
+// Selective recompute: the same GEMM also rebuilds H_i = GeLU(Y_i) from the
+// saved pre-activation it already reads, so the forward pass need not keep H.
+TPMLP_GEMM_LAUNCHER(launch_dgrad_h_recompute, false, false, EPI_DGELU_H)
 TPMLP_GEMM_LAUNCHER(launch_dgrad_x, false, false, EPI_BF16)
 }  // namespace tpmlp

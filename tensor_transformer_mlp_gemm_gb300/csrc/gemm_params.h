@@ -55,7 +55,8 @@ enum Epi : int {
     EPI_BIAS = 2,       // out 1 = bf16(acc + bias)
     EPI_DGELU = 3,      // out 1 = bf16(acc * GeLU'(in0))
     EPI_BF16 = 4,       // out 1 = bf16(acc)
-    EPI_F32 = 5         // out 1 = acc (fp32)
+    EPI_F32 = 5,        // out 1 = acc (fp32)
+    EPI_DGELU_H = 6     // out 1 = bf16(acc * GeLU'(in0)), out 2 = bf16(GeLU(in0)) (recompute)
 };
 
 // Error-word bits (which role gave up).
@@ -104,6 +105,8 @@ struct GemmParams {
 cudaError_t launch_column_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_row_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_dgrad_h(const GemmParams& p, cudaStream_t stream);
+//   dgrad_h_recompute: A K-major, B K-major, EPI_DGELU_H (dY_i and H_i = GeLU(Y_i))
+cudaError_t launch_dgrad_h_recompute(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_dgrad_x(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_wgrad(const GemmParams& p, cudaStream_t stream);
 

@@ -256,19 +256,49 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
 }
 
+// Device buffers one forward/backward pair works in.  The standard calls
+// carve them all out of one workspace; the recompute calls take the saved
+// pre-activation Y apart from a scratch area that holds the rest.
+struct Regions {
+    uint8_t* y;           // Y shards [t][T][fi] bf16 (kept from forward to backward)
+    uint8_t* h;           // H shards (kept in the standard calls; scratch with recompute)
+    uint8_t* dy;          // dY shards (scratch)
+    uint8_t* part1;       // db1 partial sums (scratch)
+    uint8_t* part2;       // db2 partial sums (scratch)
+    uint8_t* split_part;  // tail-split partial tiles (scratch)
+    uint8_t* split_cnt;   // tail-split counters (scratch)
+};
+
+Regions regions_of(uint8_t* ws, const Layout& L) {
+    return Regions{ws + L.y, ws + L.h, ws + L.dy, ws + L.part1, ws + L.part2, ws + L.split_part,
+                   ws + L.split_cnt};
+}
+
+// The recompute calls: saved = Y only; scratch = everything after Y in the
+// standard layout (H first), at the same relative offsets.
+Regions recompute_regions(uint8_t* saved, uint8_t* scratch, const Layout& L) {
+    return Regions{saved,
+                   scratch,
+                   scratch + (L.dy - L.h),
+                   scratch + (L.part1 - L.h),
+                   scratch + (L.part2 - L.h),
+                   scratch + (L.split_part - L.h),
+                   scratch + (L.split_cnt - L.h)};
+}
+
 // Workspace buffers of the tail split (see gemm_params.h).
-bool attach_split(GemmParams& p, uint8_t* ws, const Layout& L) {
+bool attach_split(GemmParams& p, const Regions& R) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(BN),
                           static_cast<cuuint64_t>(MAX_SPLIT_UNITS) * CLUSTER_M};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(BN) * 4};
     cuuint32_t box[2] = {EPI_CHUNK, 32};
     cuuint32_t estr[2] = {1, 1};
-    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ws + L.split_part, dims,
+    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, R.split_part, dims,
                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    p.partial = reinterpret_cast<const float*>(ws + L.split_part);
-    p.counters = reinterpret_cast<int*>(ws + L.split_cnt);
+    p.partial = reinterpret_cast<const float*>(R.split_part);
+    p.counters = reinterpret_cast<int*>(R.split_cnt);
     p.split_min_kblocks = g_split_min_kblocks;
     return true;
 }
@@ -291,6 +321,224 @@ Shapes shapes_of(const tpmlp_dims& d) {
 
 inline const void* shard_ptr(const void* base, int i, const Shapes& s) {
     return static_cast<const uint8_t*>(base) + static_cast<size_t>(i) * s.T * s.fi * 2;
+}
+
+// With no tokens the weight and bias gradients are zero.
+tpmlp_status zero_weight_grads(const Shapes& s, void* const* dA_shards, void* db1,
+                               void* const* dB_shards, void* db2, cudaStream_t st) {
+    const size_t wbytes = static_cast<size_t>(s.h) * s.fi * sizeof(float);
+    for (int i = 0; i < s.t; ++i) {
+        TPMLP_CUDA(cudaMemsetAsync(dA_shards[i], 0, wbytes, st));
+        TPMLP_CUDA(cudaMemsetAsync(dB_shards[i], 0, wbytes, st));
+    }
+    TPMLP_CUDA(cudaMemsetAsync(db1, 0, static_cast<size_t>(s.f) * sizeof(float), st));
+    TPMLP_CUDA(cudaMemsetAsync(db2, 0, static_cast<size_t>(s.h) * sizeof(float), st));
+    return TPMLP_OK;
+}
+
+// ---- the passes, on explicit device buffers (arguments already validated) ----------------
+
+tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* const* X,
+                         const void* const* A_shards, const void* b1,
+                         const void* const* B_shards, const void* b2, void* const* Z,
+                         const Regions& R, cudaStream_t st) {
+    const void* Y = R.y;
+    const void* H = R.h;
+
+    // column-parallel GEMM + bias + GeLU: t groups, M = T, N = fi, K = h
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_kmajor(&p.a_map[j], X[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_ROW;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
+        p.a_rows_per_map = s.Tc;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_out(&p.out_map[i], shard_ptr(Y, i, s), s.fi, s.T, false) ||
+                !encode_out(&p.out_map[MAX_MAPS + i], shard_ptr(H, i, s), s.fi, s.T, false))
+                return TPMLP_ERR_UNSUPPORTED;
+        }
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        p.bias = b1;
+        p.bias_group_stride = s.fi;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_COLUMN_FWD, 1, st,
+                         [&] { return launch_column_fwd(p, st); }));
+    }
+    // row-parallel GEMM, shard split-K + b2: M = T, N = h, K = fi per segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_kmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, BM))
+                return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi)) return TPMLP_ERR_UNSUPPORTED;
+        }
+        p.a_part = PART_KSEG;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.t;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_out(&p.out_map[j], Z[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
+        p.out_part = PART_ROW;
+        p.out_rows_per_part = s.Tc;
+        p.bias = b2;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
+                         [&] { return launch_row_fwd(p, st); }));
+    }
+    return TPMLP_OK;
+}
+
+// recompute = true: H is not read from a saved copy but rebuilt from the saved
+// Y by the dH GEMM's epilogue before the dB GEMM uses it.
+tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* const* dZ,
+                          const void* const* X, const void* const* A_shards,
+                          const void* const* B_shards, void* const* dX, void* const* dA_shards,
+                          void* db1, void* const* dB_shards, void* db2, const Regions& R,
+                          bool recompute, cudaStream_t st) {
+    const void* Y = R.y;
+    const void* H = R.h;
+    const void* dY = R.dy;
+
+    // dY_i = (dZ.B_i^T) * GeLU'(Y_i): t groups, M = T, N = fi, K = h
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_kmajor(&p.a_map[j], dZ[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_ROW;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
+        p.a_rows_per_map = s.Tc;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_out(&p.out_map[i], shard_ptr(dY, i, s), s.fi, s.T, false))
+                return TPMLP_ERR_UNSUPPORTED;
+            // selective recompute: the same epilogue rebuilds H_i = GeLU(Y_i)
+            if (recompute &&
+                !encode_out(&p.out_map[MAX_MAPS + i], shard_ptr(H, i, s), s.fi, s.T, false))
+                return TPMLP_ERR_UNSUPPORTED;
+            p.in0[i] = shard_ptr(Y, i, s);
+        }
+        p.ld_in = s.fi;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
+                         [&] {
+                             return recompute ? launch_dgrad_h_recompute(p, st)
+                                              : launch_dgrad_h(p, st);
+                         }));
+    }
+    // dX = sum_i dY_i.A_i^T: M = T, N = h, K = fi per segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        for (int i = 0; i < s.t; ++i) {
+            if (!encode_kmajor(&p.a_map[i], shard_ptr(dY, i, s), s.fi, s.T, BM))
+                return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
+        }
+        p.a_part = PART_KSEG;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.t;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_out(&p.out_map[j], dX[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
+        p.out_part = PART_ROW;
+        p.out_rows_per_part = s.Tc;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
+                         [&] { return launch_dgrad_x(p, st); }));
+    }
+    // dB_i = H_i^T.dZ: t groups, M = fi, N = h, K = Tc per chunk segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.fi, s.h, s.Tc, s.t, s.chunks);
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_GROUP;
+        p.a_nmaps = s.t;
+        p.b_nmaps = s.chunks;
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_KSEG;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_out(&p.out_map[i], dB_shards[i], s.h, s.fi, true))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
+                         [&] { return launch_wgrad(p, st); }));
+    }
+    // dA_i = X^T.dY_i: t groups, M = h, N = fi, K = Tc per chunk segment
+    {
+        GemmParams p;
+        base_params(p, *dev, s.h, s.fi, s.Tc, s.t, s.chunks);
+        for (int j = 0; j < s.chunks; ++j)
+            if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+        p.a_part = PART_KSEG;
+        p.a_nmaps = s.chunks;
+        p.b_nmaps = s.t;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.b_part = PART_GROUP;
+        p.a_rows_per_map = p.b_rows_per_map = 0;
+        for (int i = 0; i < s.t; ++i)
+            if (!encode_out(&p.out_map[i], dA_shards[i], s.fi, s.h, true))
+                return TPMLP_ERR_UNSUPPORTED;
+        p.out_part = PART_GROUP;
+        p.out_rows_per_part = 0;
+        if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
+                         [&] { return launch_wgrad(p, st); }));
+    }
+    // db1 = column sums of dY (per shard block), db2 = column sums of dZ
+    {
+        ColsumParams c1;
+        std::memset(&c1, 0, sizeof(c1));
+        for (int i = 0; i < s.t; ++i) c1.src[i] = shard_ptr(dY, i, s);
+        c1.nparts = s.t;
+        c1.rows_per_part = s.T;
+        c1.ncols = s.fi;
+        c1.mode = CS_COLS_CONCAT;
+        c1.out = static_cast<float*>(db1);
+        c1.partial = reinterpret_cast<float*>(R.part1);
+        const dim3 g1 = colsum_plan(c1, dev->sm_count);
+        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c1.splits > 1 ? 2 : 1, st,
+                         [&] { return launch_colsum(c1, g1, st, nullptr); }));
+
+        ColsumParams c2;
+        std::memset(&c2, 0, sizeof(c2));
+        for (int j = 0; j < s.chunks; ++j) c2.src[j] = dZ[j];
+        c2.nparts = s.chunks;
+        c2.rows_per_part = s.Tc;
+        c2.ncols = s.h;
+        c2.mode = CS_ROWS_CONCAT;
+        c2.out = static_cast<float*>(db2);
+        c2.partial = reinterpret_cast<float*>(R.part2);
+        const dim3 g2 = colsum_plan(c2, dev->sm_count);
+        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c2.splits > 1 ? 2 : 1, st,
+                         [&] { return launch_colsum(c2, g2, st, nullptr); }));
+    }
+    return TPMLP_OK;
 }
 
 }  // namespace
@@ -358,63 +606,9 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
     DeviceInfo* dev = nullptr;
     TPMLP_TRY(device_info(&dev));
     if (s.T == 0) return TPMLP_OK;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const Layout L = layout_of(*dims);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const void* Y = ws + L.y;
-    const void* H = ws + L.h;
-
-    // column-parallel GEMM + bias + GeLU: t groups, M = T, N = fi, K = h
-    {
-        GemmParams p;
-        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_kmajor(&p.a_map[j], X[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
-        p.a_part = PART_ROW;
-        p.a_nmaps = s.chunks;
-        p.b_nmaps = s.t;
-        p.a_rows_per_map = s.Tc;
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h)) return TPMLP_ERR_UNSUPPORTED;
-        p.b_part = PART_GROUP;
-        p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i) {
-            if (!encode_out(&p.out_map[i], shard_ptr(Y, i, s), s.fi, s.T, false) ||
-                !encode_out(&p.out_map[MAX_MAPS + i], shard_ptr(H, i, s), s.fi, s.T, false))
-                return TPMLP_ERR_UNSUPPORTED;
-        }
-        p.out_part = PART_GROUP;
-        p.out_rows_per_part = 0;
-        p.bias = b1;
-        p.bias_group_stride = s.fi;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_COLUMN_FWD, 1, st,
-                         [&] { return launch_column_fwd(p, st); }));
-    }
-    // row-parallel GEMM, shard split-K + b2: M = T, N = h, K = fi per segment
-    {
-        GemmParams p;
-        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
-        for (int i = 0; i < s.t; ++i) {
-            if (!encode_kmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, BM))
-                return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi)) return TPMLP_ERR_UNSUPPORTED;
-        }
-        p.a_part = PART_KSEG;
-        p.a_nmaps = s.t;
-        p.b_nmaps = s.t;
-        p.b_part = PART_KSEG;
-        p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_out(&p.out_map[j], Z[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
-        p.out_part = PART_ROW;
-        p.out_rows_per_part = s.Tc;
-        p.bias = b2;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
-                         [&] { return launch_row_fwd(p, st); }));
-    }
-    return TPMLP_OK;
+    return run_forward(s, dev, X, A_shards, b1, B_shards, b2, Z,
+                       regions_of(static_cast<uint8_t*>(workspace), layout_of(*dims)),
+                       static_cast<cudaStream_t>(stream));
 }
 
 TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const* dZ,
@@ -439,145 +633,78 @@ TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const*
     DeviceInfo* dev = nullptr;
     TPMLP_TRY(device_info(&dev));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (s.T == 0) {
-        const size_t wbytes = static_cast<size_t>(s.h) * s.fi * sizeof(float);
-        for (int i = 0; i < s.t; ++i) {
-            TPMLP_CUDA(cudaMemsetAsync(dA_shards[i], 0, wbytes, st));
-            TPMLP_CUDA(cudaMemsetAsync(dB_shards[i], 0, wbytes, st));
-        }
-        TPMLP_CUDA(cudaMemsetAsync(db1, 0, static_cast<size_t>(s.f) * sizeof(float), st));
-        TPMLP_CUDA(cudaMemsetAsync(db2, 0, static_cast<size_t>(s.h) * sizeof(float), st));
-        return TPMLP_OK;
-    }
+    if (s.T == 0) return zero_weight_grads(s, dA_shards, db1, dB_shards, db2, st);
+    return run_backward(s, dev, dZ, X, A_shards, B_shards, dX, dA_shards, db1, dB_shards, db2,
+                        regions_of(static_cast<uint8_t*>(workspace), layout_of(*dims)), false, st);
+}
+
+TPMLP_API tpmlp_status tpmlp_recompute_workspace_bytes(const tpmlp_dims* dims, size_t* saved_bytes,
+                                                       size_t* scratch_bytes) {
+    TPMLP_TRY(check_dims(dims));
     const Layout L = layout_of(*dims);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const void* Y = ws + L.y;
-    const void* H = ws + L.h;
-    const void* dY = ws + L.dy;
-
-    // dY_i = (dZ.B_i^T) * GeLU'(Y_i): t groups, M = T, N = fi, K = h
-    {
-        GemmParams p;
-        base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_kmajor(&p.a_map[j], dZ[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
-        p.a_part = PART_ROW;
-        p.a_nmaps = s.chunks;
-        p.b_nmaps = s.t;
-        p.a_rows_per_map = s.Tc;
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
-        p.b_part = PART_GROUP;
-        p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i) {
-            if (!encode_out(&p.out_map[i], shard_ptr(dY, i, s), s.fi, s.T, false))
-                return TPMLP_ERR_UNSUPPORTED;
-            p.in0[i] = shard_ptr(Y, i, s);
-        }
-        p.ld_in = s.fi;
-        p.out_part = PART_GROUP;
-        p.out_rows_per_part = 0;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
-                         [&] { return launch_dgrad_h(p, st); }));
-    }
-    // dX = sum_i dY_i.A_i^T: M = T, N = h, K = fi per segment
-    {
-        GemmParams p;
-        base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
-        for (int i = 0; i < s.t; ++i) {
-            if (!encode_kmajor(&p.a_map[i], shard_ptr(dY, i, s), s.fi, s.T, BM))
-                return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
-        }
-        p.a_part = PART_KSEG;
-        p.a_nmaps = s.t;
-        p.b_nmaps = s.t;
-        p.b_part = PART_KSEG;
-        p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_out(&p.out_map[j], dX[j], s.h, s.Tc, false)) return TPMLP_ERR_UNSUPPORTED;
-        p.out_part = PART_ROW;
-        p.out_rows_per_part = s.Tc;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_X, 1, st,
-                         [&] { return launch_dgrad_x(p, st); }));
-    }
-    // dB_i = H_i^T.dZ: t groups, M = fi, N = h, K = Tc per chunk segment
-    {
-        GemmParams p;
-        base_params(p, *dev, s.fi, s.h, s.Tc, s.t, s.chunks);
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T))
-                return TPMLP_ERR_UNSUPPORTED;
-        p.a_part = PART_GROUP;
-        p.a_nmaps = s.t;
-        p.b_nmaps = s.chunks;
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
-        p.b_part = PART_KSEG;
-        p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_out(&p.out_map[i], dB_shards[i], s.h, s.fi, true))
-                return TPMLP_ERR_UNSUPPORTED;
-        p.out_part = PART_GROUP;
-        p.out_rows_per_part = 0;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_B, 1, st,
-                         [&] { return launch_wgrad(p, st); }));
-    }
-    // dA_i = X^T.dY_i: t groups, M = h, N = fi, K = Tc per chunk segment
-    {
-        GemmParams p;
-        base_params(p, *dev, s.h, s.fi, s.Tc, s.t, s.chunks);
-        for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
-        p.a_part = PART_KSEG;
-        p.a_nmaps = s.chunks;
-        p.b_nmaps = s.t;
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T))
-                return TPMLP_ERR_UNSUPPORTED;
-        p.b_part = PART_GROUP;
-        p.a_rows_per_map = p.b_rows_per_map = 0;
-        for (int i = 0; i < s.t; ++i)
-            if (!encode_out(&p.out_map[i], dA_shards[i], s.fi, s.h, true))
-                return TPMLP_ERR_UNSUPPORTED;
-        p.out_part = PART_GROUP;
-        p.out_rows_per_part = 0;
-        if (!attach_split(p, ws, L)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
-                         [&] { return launch_wgrad(p, st); }));
-    }
-    // db1 = column sums of dY (per shard block), db2 = column sums of dZ
-    {
-        ColsumParams c1;
-        std::memset(&c1, 0, sizeof(c1));
-        for (int i = 0; i < s.t; ++i) c1.src[i] = shard_ptr(dY, i, s);
-        c1.nparts = s.t;
-        c1.rows_per_part = s.T;
-        c1.ncols = s.fi;
-        c1.mode = CS_COLS_CONCAT;
-        c1.out = static_cast<float*>(db1);
-        c1.partial = reinterpret_cast<float*>(ws + L.part1);
-        const dim3 g1 = colsum_plan(c1, dev->sm_count);
-        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c1.splits > 1 ? 2 : 1, st,
-                         [&] { return launch_colsum(c1, g1, st, nullptr); }));
-
-        ColsumParams c2;
-        std::memset(&c2, 0, sizeof(c2));
-        for (int j = 0; j < s.chunks; ++j) c2.src[j] = dZ[j];
-        c2.nparts = s.chunks;
-        c2.rows_per_part = s.Tc;
-        c2.ncols = s.h;
-        c2.mode = CS_ROWS_CONCAT;
-        c2.out = static_cast<float*>(db2);
-        c2.partial = reinterpret_cast<float*>(ws + L.part2);
-        const dim3 g2 = colsum_plan(c2, dev->sm_count);
-        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c2.splits > 1 ? 2 : 1, st,
-                         [&] { return launch_colsum(c2, g2, st, nullptr); }));
-    }
+    if (saved_bytes) *saved_bytes = L.h;            // the Y shards
+    if (scratch_bytes) *scratch_bytes = L.total - L.h;
     return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_forward_recompute(const tpmlp_dims* dims, const void* const* X,
+                                               const void* const* A_shards, const void* b1,
+                                               const void* const* B_shards, const void* b2,
+                                               int t, void* const* Z, void* saved, void* scratch,
+                                               void* stream) {
+    TPMLP_TRY(check_dims(dims));
+    if (t != dims->t) return TPMLP_ERR_INVALID_ARG;
+    const Shapes s = shapes_of(*dims);
+    TPMLP_TRY(check_ptrs(A_shards, s.t));
+    TPMLP_TRY(check_ptrs(B_shards, s.t));
+    TPMLP_TRY(check_ptr(b1));
+    TPMLP_TRY(check_ptr(b2));
+    if (s.T > 0) {
+        TPMLP_TRY(check_ptrs(X, s.chunks));
+        TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(Z), s.chunks));
+        TPMLP_TRY(check_ptr(saved));
+        TPMLP_TRY(check_ptr(scratch));
+    }
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    if (s.T == 0) return TPMLP_OK;
+    return run_forward(s, dev, X, A_shards, b1, B_shards, b2, Z,
+                       recompute_regions(static_cast<uint8_t*>(saved),
+                                         static_cast<uint8_t*>(scratch), layout_of(*dims)),
+                       static_cast<cudaStream_t>(stream));
+}
+
+TPMLP_API tpmlp_status tpmlp_backward_recompute(const tpmlp_dims* dims, const void* const* dZ,
+                                                const void* const* X,
+                                                const void* const* A_shards,
+                                                const void* const* B_shards, void* saved,
+                                                void* scratch, void* const* dX,
+                                                void* const* dA_shards, void* db1,
+                                                void* const* dB_shards, void* db2,
+                                                void* stream) {
+    TPMLP_TRY(check_dims(dims));
+    const Shapes s = shapes_of(*dims);
+    TPMLP_TRY(check_ptrs(A_shards, s.t));
+    TPMLP_TRY(check_ptrs(B_shards, s.t));
+    TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dA_shards), s.t));
+    TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dB_shards), s.t));
+    TPMLP_TRY(check_ptr(db1));
+    TPMLP_TRY(check_ptr(db2));
+    if (s.T > 0) {
+        TPMLP_TRY(check_ptrs(dZ, s.chunks));
+        TPMLP_TRY(check_ptrs(X, s.chunks));
+        TPMLP_TRY(check_ptrs(reinterpret_cast<const void* const*>(dX), s.chunks));
+        TPMLP_TRY(check_ptr(saved));
+        TPMLP_TRY(check_ptr(scratch));
+    }
+    DeviceInfo* dev = nullptr;
+    TPMLP_TRY(device_info(&dev));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (s.T == 0) return zero_weight_grads(s, dA_shards, db1, dB_shards, db2, st);
+    return run_backward(s, dev, dZ, X, A_shards, B_shards, dX, dA_shards, db1, dB_shards, db2,
+                        recompute_regions(static_cast<uint8_t*>(saved),
+                                          static_cast<uint8_t*>(scratch), layout_of(*dims)),
+                        true, st);
 }
 
 TPMLP_API tpmlp_status tpmlp_sync_check(void* stream) {

@@ -118,6 +118,25 @@ def test_backward_validation_codes(binding):
                               arr(one), arr(two), FAKE, arr(two), FAKE, None) == INV
 
 
+def test_recompute_workspace_and_validation(binding):
+    d = binding.make_dims(2048, 12288, 49152, 8)
+    saved, scratch = binding.tpmlp_recompute_workspace_bytes(d)
+    assert saved == 2048 * 49152 * 2                     # Y only
+    assert saved + scratch == binding.tpmlp_workspace_bytes(d)
+    lib = binding.library()
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    d = binding.make_dims(256, 256, 1024, 2)
+    two, one = [FAKE, FAKE], [FAKE]
+    INV = binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_forward_recompute(ctypes.byref(d), arr(one), arr(two), FAKE, arr(two), FAKE,
+                                       2, arr(one), None, FAKE, None) == INV  # no saved buffer
+    assert lib.tpmlp_forward_recompute(ctypes.byref(d), arr(one), arr(two), FAKE, arr(two), FAKE,
+                                       2, arr(one), FAKE, None, None) == INV  # no scratch
+    assert lib.tpmlp_backward_recompute(ctypes.byref(d), arr(one), arr(one), arr(two), arr(two),
+                                        FAKE, FAKE + 8, arr(one), arr(two), FAKE, arr(two), FAKE,
+                                        None) == binding.TPMLP_ERR_UNSUPPORTED  # misaligned
+
+
 def test_set_timeout_and_profile_args(binding):
     lib = binding.library()
     assert lib.tpmlp_set_wait_timeout_ns(0) == binding.TPMLP_ERR_INVALID_ARG
