@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the tensor-parallel Transformer MLP block.
+"""fp64 CPU oracle for the tensor-parallel Transformer MLP block and the
+column- and row-parallel linear layers it is built from.
 
 TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -63,6 +64,10 @@ def _configure(lib):
     lib.oracle_cols.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp,
                                        _i64, ctypes.POINTER(_i64), _dp, _dp, _dp]
     lib.oracle_db2.argtypes = [_i64, _i64, _dp, _dp]
+    lib.oracle_column_linear_forward.argtypes = dims + [_dp, _dpp, _dp, _dpp]
+    lib.oracle_column_linear_backward.argtypes = dims + [_dp, _dpp, _dpp, _dp, _dpp, _dp]
+    lib.oracle_row_linear_forward.argtypes = dims + [_dpp, _dpp, _dp, _dp]
+    lib.oracle_row_linear_backward.argtypes = dims + [_dpp, _dpp, _dp, _dpp, _dpp, _dp]
     return lib
 
 
@@ -241,4 +246,53 @@ def forward_backward_sp(X_chunks, A_shards, b1, B_shards, b2, dZ_chunks):
     out = forward_backward(sp_gather(X_chunks), A_shards, b1, B_shards, b2, sp_gather(dZ_chunks))
     out["Z_chunks"] = sp_scatter(out["Z"], n)
     out["dX_chunks"] = sp_scatter(out["dX"], n)
+    return out
+
+
+# ---- tensor-parallel linear layers (attention projections) -------------------
+# Column parallel: Y_i = X.W_i + b_i; row parallel: Z = sum_i X_i.W_i + b
+# ("2、分布式训练基础…", 2.2 模型并行 —— 张量并行 / 核心原理).
+
+def column_linear(X, W_shards, b, dY_shards=None):
+    """Forward Y_i (list), and with dY_i given the backward dX, dW_i, db."""
+    lib = _load()
+    X = _f64(X); b = _f64(b); W = [_f64(w) for w in W_shards]
+    t = len(W); T, din = X.shape; oi = W[0].shape[1]; dout = t * oi
+    if any(w.shape != (din, oi) for w in W) or b.shape != (dout,):
+        raise ValueError("W_i must be [in, out/t] and b [out]")
+    Y = [np.empty((T, oi)) for _ in range(t)]
+    keep = []
+    def P(lst):
+        p, k = _ptrs(lst); keep.append(k); return p
+    lib.oracle_column_linear_forward(T, din, dout, t, _ptr(X), P(W), _ptr(b), P(Y))
+    out = {"Y": Y}
+    if dY_shards is not None:
+        dY = [_f64(d) for d in dY_shards]
+        dX = np.empty((T, din)); dW = [np.empty((din, oi)) for _ in range(t)]; db = np.empty(dout)
+        lib.oracle_column_linear_backward(T, din, dout, t, _ptr(X), P(W), P(dY), _ptr(dX),
+                                          P(dW), _ptr(db))
+        out.update(dX=dX, dW=dW, db=db)
+    return out
+
+
+def row_linear(X_shards, W_shards, b, dZ=None):
+    """Forward Z, and with dZ given the backward dX_i (list), dW_i, db."""
+    lib = _load()
+    X = [_f64(x) for x in X_shards]; W = [_f64(w) for w in W_shards]; b = _f64(b)
+    t = len(W); T, ii = X[0].shape; dout = W[0].shape[1]; din = t * ii
+    if any(w.shape != (ii, dout) for w in W) or any(x.shape != (T, ii) for x in X):
+        raise ValueError("X_i must be [T, in/t] and W_i [in/t, out]")
+    Z = np.empty((T, dout))
+    keep = []
+    def P(lst):
+        p, k = _ptrs(lst); keep.append(k); return p
+    lib.oracle_row_linear_forward(T, din, dout, t, P(X), P(W), _ptr(b), _ptr(Z))
+    out = {"Z": Z}
+    if dZ is not None:
+        dZ = _f64(dZ)
+        dX = [np.empty((T, ii)) for _ in range(t)]; dW = [np.empty((ii, dout)) for _ in range(t)]
+        db = np.empty(dout)
+        lib.oracle_row_linear_backward(T, din, dout, t, P(X), P(W), _ptr(dZ), P(dX), P(dW),
+                                       _ptr(db))
+        out.update(dX=dX, dW=dW, db=db)
     return out

@@ -36,6 +36,11 @@
  *       dA_i = X^T.dY_i, dB_i = H_i^T.dZ, db1 = column sums of dY,
  *       db2 = column sums of dZ.
  *
+ *   - The attention projections are the same two halves without the GeLU
+ *     ([CH2] 2.2: the QKV projection column parallel, the output projection
+ *     row parallel); their biases follow the same placement as b1 and b2.
+ *     Pinned by tests/test_oracle_linear_pins.py.
+ *
  * Parallelism: OpenMP over output rows only; every output element is a
  * plain sum taken in index order.
  */
@@ -320,5 +325,134 @@ void oracle_db2(int64_t T, int64_t h, const double *dZ, double *db2) {
         double s = 0.0;
         for (int64_t r = 0; r < T; ++r) s += dZ[r * h + n];
         db2[n] = s;
+    }
+}
+
+/* ---- tensor-parallel linear layers ------------------------------------------
+ * The two halves of the block without the GeLU, as used for the attention
+ * projections ([CH2] 2.2: QKV projection column parallel, output projection
+ * row parallel; [FGO] 张量并行原理).  in = input width, out = output width.
+ *
+ * Column parallel, W split by columns into t shards W_i [in, oi], oi = out/t:
+ *   Y_i = X.W_i + b[i*oi:(i+1)*oi]                     Y_i [T, oi]
+ * backward for upstream dY_i:
+ *   dX = sum_i dY_i.W_i^T, dW_i = X^T.dY_i, db = column sums of [dY_1..dY_t]
+ */
+void oracle_column_linear_forward(int64_t T, int64_t in, int64_t out, int t,
+                                  const double *X, const double *const *W,
+                                  const double *b, double *const *Y) {
+    const int64_t oi = out / t;
+    for (int i = 0; i < t; ++i) {
+        const double *Wi = W[i];
+        double *Yi = Y[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < T; ++r) {
+            double *yrow = Yi + r * oi;
+            for (int64_t j = 0; j < oi; ++j) yrow[j] = 0.0;
+            for (int64_t k = 0; k < in; ++k) {
+                const double x = X[r * in + k];
+                const double *wrow = Wi + k * oi;
+                for (int64_t j = 0; j < oi; ++j) yrow[j] += x * wrow[j];
+            }
+            for (int64_t j = 0; j < oi; ++j) yrow[j] += b[i * oi + j];
+        }
+    }
+}
+
+void oracle_column_linear_backward(int64_t T, int64_t in, int64_t out, int t,
+                                   const double *X, const double *const *W,
+                                   const double *const *dY, double *dX,
+                                   double *const *dW, double *db) {
+    const int64_t oi = out / t;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        for (int64_t k = 0; k < in; ++k) {
+            double acc = 0.0;
+            for (int i = 0; i < t; ++i) {
+                const double *wrow = W[i] + k * oi;
+                const double *dyrow = dY[i] + r * oi;
+                for (int64_t j = 0; j < oi; ++j) acc += dyrow[j] * wrow[j];
+            }
+            dX[r * in + k] = acc;
+        }
+    }
+    for (int i = 0; i < t; ++i) {
+        const double *dYi = dY[i];
+        double *dWi = dW[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t k = 0; k < in; ++k) {
+            double *o = dWi + k * oi;
+            for (int64_t j = 0; j < oi; ++j) o[j] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                const double x = X[r * in + k];
+                const double *dyrow = dYi + r * oi;
+                for (int64_t j = 0; j < oi; ++j) o[j] += x * dyrow[j];
+            }
+        }
+        for (int64_t j = 0; j < oi; ++j) {
+            double s = 0.0;
+            for (int64_t r = 0; r < T; ++r) s += dYi[r * oi + j];
+            db[i * oi + j] = s;
+        }
+    }
+}
+
+/* Row parallel, W split by rows into t shards W_i [ii, out], ii = in/t, and
+ * the input split by columns into X_i [T, ii]:
+ *   Z = (sum_i X_i.W_i) + b                            Z [T, out]
+ * backward for upstream dZ:
+ *   dX_i = dZ.W_i^T, dW_i = X_i^T.dZ, db = column sums of dZ
+ */
+void oracle_row_linear_forward(int64_t T, int64_t in, int64_t out, int t,
+                               const double *const *X, const double *const *W,
+                               const double *b, double *Z) {
+    const int64_t ii = in / t;
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        double *zrow = Z + r * out;
+        for (int64_t n = 0; n < out; ++n) zrow[n] = 0.0;
+        for (int i = 0; i < t; ++i) {
+            for (int64_t k = 0; k < ii; ++k) {
+                const double x = X[i][r * ii + k];
+                const double *wrow = W[i] + k * out;
+                for (int64_t n = 0; n < out; ++n) zrow[n] += x * wrow[n];
+            }
+        }
+        for (int64_t n = 0; n < out; ++n) zrow[n] += b[n];
+    }
+}
+
+void oracle_row_linear_backward(int64_t T, int64_t in, int64_t out, int t,
+                                const double *const *X, const double *const *W,
+                                const double *dZ, double *const *dX,
+                                double *const *dW, double *db) {
+    const int64_t ii = in / t;
+    for (int i = 0; i < t; ++i) {
+        const double *Wi = W[i], *Xi = X[i];
+        double *dXi = dX[i], *dWi = dW[i];
+        #pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < T; ++r) {
+            for (int64_t k = 0; k < ii; ++k) {
+                double acc = 0.0;
+                const double *wrow = Wi + k * out;
+                for (int64_t n = 0; n < out; ++n) acc += dZ[r * out + n] * wrow[n];
+                dXi[r * ii + k] = acc;
+            }
+        }
+        #pragma omp parallel for schedule(static)
+        for (int64_t k = 0; k < ii; ++k) {
+            double *o = dWi + k * out;
+            for (int64_t n = 0; n < out; ++n) o[n] = 0.0;
+            for (int64_t r = 0; r < T; ++r) {
+                const double x = Xi[r * ii + k];
+                const double *dzrow = dZ + r * out;
+                for (int64_t n = 0; n < out; ++n) o[n] += x * dzrow[n];
+            }
+        }
+    }
+    for (int64_t n = 0; n < out; ++n) {
+        double s = 0.0;
+        for (int64_t r = 0; r < T; ++r) s += dZ[r * out + n];
+        db[n] = s;
     }
 }

@@ -7,6 +7,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_linear_pins as lin
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -28,6 +29,20 @@ MUTATIONS = [
     ("db1 sign", "db1[i * fi + j] = s;", "db1[i * fi + j] = -s;"),
     ("dH uses dZ transposed", "for (int64_t n = 0; n < h; ++n) dh += dZ[r * h + n] * brow[n];\n                dYi",
      "for (int64_t n = 0; n < h; ++n) dh += dZ[(n % T) * h + (r % h)] * brow[n];\n                dYi"),
+    # tensor-parallel linear layers
+    ("column linear: bias of shard 0", "yrow[j] += b[i * oi + j];", "yrow[j] += b[j];"),
+    ("column linear: dX drops last shard", "for (int i = 0; i < t; ++i) {\n                const double *wrow = W[i]",
+     "for (int i = 0; i + 1 < t; ++i) {\n                const double *wrow = W[i]"),
+    ("column linear: dW pairs tokens in reverse", "const double *dyrow = dYi + r * oi;\n                for (int64_t j = 0; j < oi; ++j) o[j]",
+     "const double *dyrow = dYi + (T - 1 - r) * oi;\n                for (int64_t j = 0; j < oi; ++j) o[j]"),
+    ("column linear: db sign", "db[i * oi + j] = s;", "db[i * oi + j] = -s;"),
+    ("row linear: bias twice", "zrow[n] += b[n];", "zrow[n] += 2.0 * b[n];"),
+    ("row linear: dX skips last output column", "for (int64_t n = 0; n < out; ++n) acc += dZ[r * out + n] * wrow[n];",
+     "for (int64_t n = 0; n + 1 < out; ++n) acc += dZ[r * out + n] * wrow[n];"),
+    ("row linear: dW drops first token", "for (int64_t r = 0; r < T; ++r) {\n                const double x = Xi[r * ii + k];",
+     "for (int64_t r = 1; r < T; ++r) {\n                const double x = Xi[r * ii + k];"),
+    ("row linear: db from the first row only", "for (int64_t r = 0; r < T; ++r) s += dZ[r * out + n];",
+     "for (int64_t r = 0; r < 1; ++r) s += dZ[r * out + n];"),
 ]
 
 PIN_CALLS = [
@@ -36,6 +51,8 @@ PIN_CALLS = [
     lambda: pins.test_random_block_against_numpy(7, 5, 12, 3),
     lambda: pins.test_gelu_closed_form(),
     lambda: pins.test_b2_added_once(),
+    lambda: lin.test_column_linear_exact_integers(3, 4, 6, 2),
+    lambda: lin.test_row_linear_exact_integers(3, 6, 4, 2),
 ]
 
 
