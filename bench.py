@@ -10,6 +10,12 @@ gradients) over one batch of seeded synthetic input of the named workload
 value is fwd+bwd TFLOP/s (12*T*h*f FLOP per step) over all ranks; tokens/s and
 the fraction of the dense bf16 peak ride along.  Prints one JSON line.
 
+--workload may also name one of the tensor-parallel linear layers (the
+attention projections, e.g. qkv_175b: the 175B-class QKV projection 12288 x
+36864, column parallel, t=8; attn_out_175b: its 12288 x 12288 output
+projection, row parallel).  One step is then that layer's forward and
+backward (3 GEMMs of 2*T*in*out FLOP and the bias gradient).
+
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded token sample of the same layer per step (same metric and unit).
 Under torchrun with N > 1 every rank runs an independent replica of the
@@ -30,6 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300; % of BF16 dense peak"
+LINEAR_METRIC = ("TP linear layer (attention projection) fwd+bwd TFLOP/s and tokens/s on 1 GB300; "
+                 "% of BF16 dense peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -78,6 +86,27 @@ def pick_workload(args):
     return w
 
 
+def pick_linear_workload(args):
+    from dataclasses import replace
+    from tensor_transformer_mlp_gemm_gb300.inputs import LINEAR_WORKLOADS
+    w = LINEAR_WORKLOADS[args.workload]
+    over = {}
+    if args.tokens is not None:
+        over["tokens"] = args.tokens
+    if args.t is not None:
+        over["t"] = args.t
+        over["seq_chunks"] = min(w.seq_chunks, args.t)
+    if over:
+        w = replace(w, name=w.name + "(" + ",".join(f"{k}={v}" for k, v in over.items()) + ")",
+                    **over)
+    return w
+
+
+def is_linear(args) -> bool:
+    from tensor_transformer_mlp_gemm_gb300.inputs import LINEAR_WORKLOADS
+    return args.workload in LINEAR_WORKLOADS
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -118,6 +147,14 @@ def workload_config(w, l2_note):
                         f"h={w.hidden}, f={w.ffn}, t={w.t}, seq_chunks={w.seq_chunks}",
             "tokens": w.tokens, "hidden": w.hidden, "ffn": w.ffn, "t": w.t,
             "seq_chunks": w.seq_chunks, "sigma_w": w.sigma_w, "seed": 0, "l2": l2_note}
+
+
+def linear_config(w, l2_note):
+    return {"workload": f"{w.name}: {w.split}-parallel linear, T={w.tokens}, in={w.in_features}, "
+                        f"out={w.out_features}, t={w.t}, seq_chunks={w.seq_chunks}",
+            "tokens": w.tokens, "in_features": w.in_features, "out_features": w.out_features,
+            "split": w.split, "t": w.t, "seq_chunks": w.seq_chunks, "sigma_w": w.sigma_w,
+            "seed": 0, "l2": l2_note}
 
 
 # ---- clocks -----------------------------------------------------------------------------
@@ -235,15 +272,66 @@ class OracleSample:
         return max(1, min(cap, want))
 
 
+    def flops(self, tokens: int) -> float:
+        return 12.0 * tokens * self.w.hidden * self.w.ffn
+
+    def describe(self) -> str:
+        return f"h={self.w.hidden}, f={self.w.ffn}, t={self.w.t}"
+
+
+class LinearOracleSample(OracleSample):
+    """The fp64 oracle of a linear layer on the first T_s tokens (same weights)."""
+
+    def __init__(self, w, inputs):
+        import numpy as np
+        import oracle
+        from tensor_transformer_mlp_gemm_gb300.inputs import column_shards, row_shards
+        self.oracle = oracle
+        self.cores = len(os.sched_getaffinity(0))
+        oracle.set_threads(self.cores)
+        self.w = w
+        f64 = lambda x: np.ascontiguousarray(x.double().numpy())
+        if w.split == "column":
+            self.W = [f64(x) for x in column_shards(inputs["W"], w.t)]
+            self.X = f64(inputs["X"])
+            self.dY = [f64(x) for x in column_shards(inputs["dY"], w.t)]
+        else:
+            self.W = [f64(x) for x in row_shards(inputs["W"], w.t)]
+            self.X = [f64(x) for x in column_shards(inputs["X"], w.t)]
+            self.dY = f64(inputs["dY"])
+        self.b = f64(inputs["b"])
+
+    def run(self, tokens: int) -> float:
+        t0 = time.perf_counter()
+        if self.w.split == "column":
+            self.oracle.column_linear(self.X[:tokens], self.W, self.b,
+                                      [d[:tokens] for d in self.dY])
+        else:
+            self.oracle.row_linear([x[:tokens] for x in self.X], self.W, self.b,
+                                   self.dY[:tokens])
+        return time.perf_counter() - t0
+
+    def flops(self, tokens: int) -> float:
+        return 6.0 * tokens * self.w.in_features * self.w.out_features
+
+    def describe(self) -> str:
+        w = self.w
+        return f"{w.split} split, in={w.in_features}, out={w.out_features}, t={w.t}"
+
+
+def oracle_sample(w, inputs):
+    return LinearOracleSample(w, inputs) if hasattr(w, "split") else OracleSample(w, inputs)
+
+
 def cpu_baseline(w, inputs, target_s: float) -> dict:
-    smp = OracleSample(w, inputs)
+    smp = oracle_sample(w, inputs)
     tok = smp.calibrate(target_s)
     dt = smp.run(tok)
-    flops = 12.0 * tok * w.hidden * w.ffn
+    flops = smp.flops(tok)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": smp.cores, "kind": "oracle",
             "tokens_per_s": tok / dt, "seconds": dt,
             "sample": f"fp64 oracle fwd+bwd on the first {tok} of {w.tokens} tokens of the same "
-                      f"layer (h={w.hidden}, f={w.ffn}, t={w.t}), same weights; "
+                      f"layer ({smp.describe()}), same weights; "
                       f"{flops / 1e9:.1f} GFLOP in {dt:.1f} s"}
 
 
@@ -289,9 +377,16 @@ def run_reference(args, torch):
         if dist is not None:
             dist.destroy_process_group()
         return
-    w = pick_workload(args)
-    inputs = make_inputs(w, 0)
-    smp = OracleSample(w, inputs)
+    if is_linear(args):
+        from tensor_transformer_mlp_gemm_gb300.inputs import make_linear_inputs
+        w = pick_linear_workload(args)
+        inputs = make_linear_inputs(w, 0)
+        metric, config = LINEAR_METRIC, linear_config(w, "host memory (CPU oracle)")
+    else:
+        w = pick_workload(args)
+        inputs = make_inputs(w, 0)
+        metric, config = METRIC, workload_config(w, "host memory (CPU oracle)")
+    smp = oracle_sample(w, inputs)
     per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
     tok = smp.calibrate(per_step, start=min(w.tokens, max(4, smp.cores // 2)))
     for _ in range(args.warmup):
@@ -300,13 +395,13 @@ def run_reference(args, torch):
     for _ in range(args.steps):
         smp.run(tok)
     dt = time.perf_counter() - t0
-    flops = 12.0 * tok * w.hidden * w.ffn * args.steps
+    flops = smp.flops(tok) * args.steps
     value = flops / dt / 1e12
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, "host memory (CPU oracle)"),
+            "config": config,
             "tokens_per_s": tok * args.steps / dt,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": smp.cores,
                              "kind": "oracle",
@@ -319,6 +414,97 @@ def run_reference(args, torch):
         dist.destroy_process_group()
 
 
+class MlpRunner:
+    """One step = tpmlp_forward + tpmlp_backward of the MLP block."""
+
+    def __init__(self, args, dev):
+        from tensor_transformer_mlp_gemm_gb300 import binding
+        from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
+        from tensor_transformer_mlp_gemm_gb300.inputs import make_inputs
+        self.binding = binding
+        self.w = w = pick_workload(args)
+        self.inputs = make_inputs(w, 0)
+        self.recompute = bool(args.recompute)
+        self.blk = DeviceBlock(w, self.inputs, device=dev, recompute=args.recompute)
+        T, h, f = w.tokens, w.hidden, w.ffn
+        self.tokens = T
+        self.metric = METRIC
+        self.flops_step = 12.0 * T * h * f
+        self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
+        self.gemm_flops = 2.0 * T * h * f  # every GEMM launch
+        # column sums: read dY [T, f] and dZ [T, h] bf16, write db1, db2 fp32, per step
+        self.colsum_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
+        self.l2_note = (f"inputs larger than L2 (bf16 weights {2 * h * f * 2 / 1e9:.2f} GB, "
+                        f"activations {3 * T * f * 2 / 1e9:.2f} GB per step)")
+        self.ins, self.outs = ("X", "dZ"), ("Z", "dX")  # per-step uploads; fwd, bwd results
+
+    def config(self):
+        return {**workload_config(self.w, self.l2_note),
+                "activation_recompute": self.recompute}
+
+    def buffers(self, name):
+        return getattr(self.blk, name)
+
+    def step(self, stream):
+        self.blk.step(stream)
+
+    def forward(self, B, stream):
+        b, blk, w = self.binding, self.blk, self.w
+        if self.recompute:
+            b.tpmlp_forward_recompute(blk.dims, B["X"], blk.A, blk.b1, blk.B, blk.b2, w.t, B["Z"],
+                                      blk.saved_y, blk.scratch, stream)
+        else:
+            b.tpmlp_forward(blk.dims, B["X"], blk.A, blk.b1, blk.B, blk.b2, w.t, B["Z"], blk.ws,
+                            stream)
+
+    def backward(self, B, stream):
+        b, blk = self.binding, self.blk
+        if self.recompute:
+            b.tpmlp_backward_recompute(blk.dims, B["dZ"], B["X"], blk.A, blk.B, blk.saved_y,
+                                       blk.scratch, B["dX"], blk.dA, blk.db1, blk.dB, blk.db2,
+                                       stream)
+        else:
+            b.tpmlp_backward(blk.dims, B["dZ"], B["X"], blk.A, blk.B, blk.ws, B["dX"], blk.dA,
+                             blk.db1, blk.dB, blk.db2, stream)
+
+
+class LinearRunner:
+    """One step = forward + backward of one tensor-parallel linear layer."""
+
+    def __init__(self, args, dev):
+        from tensor_transformer_mlp_gemm_gb300.inputs import make_linear_inputs
+        from tensor_transformer_mlp_gemm_gb300.linear import DeviceLinear
+        self.w = w = pick_linear_workload(args)
+        self.inputs = make_linear_inputs(w, 0)
+        self.lin = DeviceLinear(w, self.inputs, device=dev)
+        T, din, dout = w.tokens, w.in_features, w.out_features
+        self.tokens = T
+        self.metric = LINEAR_METRIC
+        self.flops_step = 6.0 * T * din * dout
+        self.gemm_kinds = ("linear_fwd", "linear_dgrad", "linear_wgrad")
+        self.gemm_flops = 2.0 * T * din * dout
+        # column sums: read dY [T, out] bf16, write db fp32, per step
+        self.colsum_bytes = T * dout * 2 + dout * 4
+        self.l2_note = (f"inputs larger than L2 (bf16 weight {din * dout * 2 / 1e9:.2f} GB, "
+                        f"activations {T * (din + 2 * dout) * 2 / 1e9:.2f} GB per step)")
+        self.ins, self.outs = ("X", "dY"), ("Y", "dX")
+
+    def config(self):
+        return linear_config(self.w, self.l2_note)
+
+    def buffers(self, name):
+        return getattr(self.lin, name)
+
+    def step(self, stream):
+        self.lin.step(stream)
+
+    def forward(self, B, stream):
+        self.lin.forward(stream, X=B["X"], Y=B["Y"])
+
+    def backward(self, B, stream):
+        self.lin.backward(stream, dY=B["dY"], X=B["X"], dX=B["dX"])
+
+
 def run_ours(args, torch):
     from tensor_transformer_mlp_gemm_gb300.build import build
     dist, rank, world, local = dist_setup(torch)
@@ -327,26 +513,20 @@ def run_ours(args, torch):
     if dist is not None:
         dist.barrier()
     from tensor_transformer_mlp_gemm_gb300 import binding
-    from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
-    from tensor_transformer_mlp_gemm_gb300.inputs import make_inputs
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.split_min_kblocks is not None:
         binding.tpmlp_set_split_min_kblocks(args.split_min_kblocks)
-    w = pick_workload(args)
-    inputs = make_inputs(w, 0)
-    blk = DeviceBlock(w, inputs, device=dev, recompute=args.recompute)
+    run = LinearRunner(args, dev) if is_linear(args) else MlpRunner(args, dev)
+    w = run.w
     stream = torch.cuda.current_stream(dev)
-    T, h, f = w.tokens, w.hidden, w.ffn
-    flops_step = 12.0 * T * h * f
-    weight_bytes = 2 * h * f * 2
-    l2_note = (f"inputs larger than L2 (bf16 weights {weight_bytes / 1e9:.2f} GB, "
-               f"activations {3 * T * f * 2 / 1e9:.2f} GB per step)")
+    T = run.tokens
+    flops_step = run.flops_step
 
     # warm-up, then the timed device-resident loop
     for _ in range(args.warmup):
-        blk.step(stream)
+        run.step(stream)
     st = binding.tpmlp_sync_check(stream)
     if st != binding.TPMLP_OK:
         raise RuntimeError(f"warm-up failed: {binding.tpmlp_status_string(st)}")
@@ -360,7 +540,7 @@ def run_ours(args, torch):
     barrier(dist, torch)
     e0.record(stream)
     for _ in range(args.steps):
-        blk.step(stream)
+        run.step(stream)
     e1.record(stream)
     barrier(dist, torch)
     kms, kcount = binding.tpmlp_profile_end()
@@ -380,10 +560,9 @@ def run_ours(args, torch):
         if kcount[name]:
             kernels[name] = {"launches": kcount[name], "ms_per_launch": kms[name] / kcount[name],
                              "share": kms[name] / total_k if total_k else None}
-    gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
     dom = max(kernels, key=lambda k: kms[k])
-    if dom in gemm_kinds:
-        achieved = 2.0 * T * h * f / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
+    if dom in run.gemm_kinds:
+        achieved = run.gemm_flops / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops_sustained"],
@@ -391,41 +570,39 @@ def run_ours(args, torch):
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long "
                                f"step); frac of burst {peaks['bf16_tflops']}: "
                                f"{achieved / peaks['bf16_tflops']:.3f}",
-                "flops_per_launch": 2.0 * T * h * f}
+                "flops_per_launch": run.gemm_flops}
     else:
-        gb = (T * f * 2 + T * h * 2) / 1e9
-        achieved = gb / (kms[dom] / kcount[dom] / 1e3)
+        achieved = run.colsum_bytes / 1e9 / (kms[dom] / args.steps / 1e3)
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None}
     if "bias_grad" in kernels:
-        # column sums: read dY [T, f] and dZ [T, h] bf16, write db1, db2 fp32, per step
-        cs_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
         cs_ms = kms["bias_grad"] / args.steps
-        kernels["bias_grad"]["gb_per_s"] = cs_bytes / (cs_ms / 1e3) / 1e9
+        kernels["bias_grad"]["gb_per_s"] = run.colsum_bytes / (cs_ms / 1e3) / 1e9
         kernels["bias_grad"]["frac_of_hbm"] = kernels["bias_grad"]["gb_per_s"] / peaks["hbm_gbs"]
-    for name in gemm_kinds:
+    for name in run.gemm_kinds:
         if name in kernels:
-            kernels[name]["tflops"] = 2.0 * T * h * f / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
+            kernels[name]["tflops"] = run.gemm_flops / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
     launches_per_step = sum(kcount.values()) / args.steps
 
     # End to end through the C ABI with host buffers.  Every step uploads its
-    # X and dZ from pinned host memory and downloads its Z and dX.  The copies
-    # run on a second stream with double-buffered device activations, so the
+    # inputs (the block: X and dZ; a linear layer: X and dY) from pinned host
+    # memory and downloads its forward and backward results.  The copies run
+    # on a second stream with double-buffered device activations, so the
     # upload of step i+1 and the downloads of step i overlap step i's GEMMs, as
     # a training loop that prefetches its next batch would.
     e2e = None
     if not args.no_e2e:
         copy_stream = torch.cuda.Stream(dev)
-        hX = [x.cpu().pin_memory() for x in blk.X]
-        hdZ = [x.cpu().pin_memory() for x in blk.dZ]
-        hZ = [torch.empty_like(z, device="cpu").pin_memory() for z in blk.Z]
-        hdX = [torch.empty_like(z, device="cpu").pin_memory() for z in blk.dX]
+        names = run.ins + run.outs
+        host_in = {k: [x.cpu().pin_memory() for x in run.buffers(k)] for k in run.ins}
+        host_out = {k: [torch.empty_like(x, device="cpu").pin_memory() for x in run.buffers(k)]
+                    for k in run.outs}
         bufs = []
         for b in range(2):
-            bufs.append({k: [torch.empty_like(x) for x in getattr(blk, k)]
-                         for k in ("X", "dZ", "Z", "dX")})
+            bufs.append({k: [torch.empty_like(x) for x in run.buffers(k)] for k in names})
         ev = {k: [torch.cuda.Event() for _ in range(2)]
               for k in ("in_ready", "fwd_done", "bwd_done", "out_done")}
+        fwd_out, bwd_out = run.outs
 
         def e2e_steps(n):
             for i in range(n):
@@ -434,34 +611,21 @@ def run_ours(args, torch):
                 with torch.cuda.stream(copy_stream):
                     if i >= 2:  # step i-2 is done with this buffer set
                         copy_stream.wait_event(ev["out_done"][b])
-                    for d, h in zip(B["X"], hX):
-                        d.copy_(h, non_blocking=True)
-                    for d, h in zip(B["dZ"], hdZ):
-                        d.copy_(h, non_blocking=True)
+                    for k in run.ins:
+                        for d, h in zip(B[k], host_in[k]):
+                            d.copy_(h, non_blocking=True)
                     ev["in_ready"][b].record(copy_stream)
                 stream.wait_event(ev["in_ready"][b])
-                if args.recompute:
-                    binding.tpmlp_forward_recompute(blk.dims, B["X"], blk.A, blk.b1, blk.B,
-                                                    blk.b2, w.t, B["Z"], blk.saved_y,
-                                                    blk.scratch, stream)
-                else:
-                    binding.tpmlp_forward(blk.dims, B["X"], blk.A, blk.b1, blk.B, blk.b2, w.t,
-                                          B["Z"], blk.ws, stream)
+                run.forward(B, stream)
                 ev["fwd_done"][b].record(stream)
-                if args.recompute:
-                    binding.tpmlp_backward_recompute(blk.dims, B["dZ"], B["X"], blk.A, blk.B,
-                                                     blk.saved_y, blk.scratch, B["dX"], blk.dA,
-                                                     blk.db1, blk.dB, blk.db2, stream)
-                else:
-                    binding.tpmlp_backward(blk.dims, B["dZ"], B["X"], blk.A, blk.B, blk.ws,
-                                           B["dX"], blk.dA, blk.db1, blk.dB, blk.db2, stream)
+                run.backward(B, stream)
                 ev["bwd_done"][b].record(stream)
                 with torch.cuda.stream(copy_stream):
                     copy_stream.wait_event(ev["fwd_done"][b])
-                    for h, d in zip(hZ, B["Z"]):
+                    for h, d in zip(host_out[fwd_out], B[fwd_out]):
                         h.copy_(d, non_blocking=True)
                     copy_stream.wait_event(ev["bwd_done"][b])
-                    for h, d in zip(hdX, B["dX"]):
+                    for h, d in zip(host_out[bwd_out], B[bwd_out]):
                         h.copy_(d, non_blocking=True)
                     ev["out_done"][b].record(copy_stream)
 
@@ -479,13 +643,16 @@ def run_ours(args, torch):
         st = binding.tpmlp_sync_check(stream)
         if st != binding.TPMLP_OK:
             raise RuntimeError(f"e2e loop failed: {binding.tpmlp_status_string(st)}")
-        if not (torch.equal(hZ[0], blk.Z[0].cpu()) and torch.equal(hdX[0], blk.dX[0].cpu())):
-            raise RuntimeError("e2e outputs differ from the device-resident step")
+        for k in run.outs:
+            if not torch.equal(host_out[k][0], run.buffers(k)[0].cpu()):
+                raise RuntimeError(f"e2e output {k} differs from the device-resident step")
         ms_e2e = max_over_ranks(dist, torch, e2.elapsed_time(e3))
         e2e = {"value": flops_step * args.e2e_steps * world / (ms_e2e / 1e3) / 1e12,
                "unit": "TFLOP/s",
-               "h2d_bytes_per_step": sum(x.numel() * 2 for x in hX + hdZ),
-               "d2h_bytes_per_step": sum(x.numel() * 2 for x in hZ + hdX),
+               "h2d_bytes_per_step": sum(x.numel() * x.element_size()
+                                         for k in run.ins for x in host_in[k]),
+               "d2h_bytes_per_step": sum(x.numel() * x.element_size()
+                                         for k in run.outs for x in host_out[k]),
                "tokens_per_s": T * args.e2e_steps * world / (ms_e2e / 1e3),
                "steps": args.e2e_steps,
                "overlap": "copies on a second stream, double-buffered activations"}
@@ -493,13 +660,12 @@ def run_ours(args, torch):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(w, inputs, args.cpu_seconds)
-        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            cpu = cpu_baseline(w, run.inputs, args.cpu_seconds)
+        line = {"metric": run.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {**workload_config(w, l2_note),
-                           "activation_recompute": bool(args.recompute)},
+                "config": run.config(),
                 "tokens_per_s": tokens_s,
                 "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
                                      "sustained": value / world / peaks["bf16_tflops_sustained"],

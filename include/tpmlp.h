@@ -1,6 +1,7 @@
 /*
  * tpmlp.h -- C ABI of libtpmlp: the tensor-parallel Transformer MLP block,
- * forward and backward, on one sm_103 GPU.
+ * forward and backward, on one sm_103 GPU, and the column- and row-parallel
+ * linear layers it is made of (the attention projections).
  *
  *     Z = GeLU(X.A + b1).B + b2
  *
@@ -168,6 +169,85 @@ tpmlp_status tpmlp_backward_recompute(const tpmlp_dims* dims,
                                       void* const* dB_shards, void* db2,
                                       void* stream);
 
+/* ---- Tensor-parallel linear layers ------------------------------------------
+ * The two halves of the block without the GeLU, as the attention projections
+ * use them ([CH2] 2.2: the QKV projection is column parallel, the output
+ * projection row parallel; [FGO] 张量并行原理).  Same kernels, conventions,
+ * sequence-parallel chunking and error behaviour as tpmlp_forward /
+ * tpmlp_backward.  Notation: T = tokens, in = in_features, out =
+ * out_features, Tc = T / seq_chunks.
+ *
+ * Requirements (else TPMLP_ERR_UNSUPPORTED) as for the block, with:
+ *   column parallel: t divides out (else TPMLP_ERR_INVALID_ARG); in and
+ *                    oi = out / t multiples of 8;
+ *   row parallel:    t divides in (else TPMLP_ERR_INVALID_ARG); ii = in / t
+ *                    and out multiples of 8.
+ * The workspace holds only scratch (tail-split partial tiles, bias-gradient
+ * partial sums); nothing in it lives from one call to the next, so one
+ * workspace may serve every linear layer that runs on one stream. */
+typedef struct {
+    int64_t tokens;        /* T */
+    int64_t in_features;   /* in: K of the forward product */
+    int64_t out_features;  /* out: N of the forward product */
+    int32_t t;             /* shards (1..8): of out (column) or of in (row) */
+    int32_t seq_chunks;    /* 1, or the sequence-parallel degree */
+} tpmlp_linear_dims;
+
+/* Bytes of scratch workspace any linear-layer call with these dims needs. */
+size_t tpmlp_linear_workspace_bytes(const tpmlp_linear_dims* dims);
+
+/* Column-parallel forward:  Y_i = X.W_i + b[i*oi:(i+1)*oi]
+ *   X        [seq_chunks] chunks of [Tc, in] bf16 (gathered on the fly)
+ *   W_shards [t] of [in, oi] bf16 (column block i of W)
+ *   b        [out] bf16
+ *   Y_shards [t] of [T, oi] bf16 (output)
+ * Backward for upstream dY_i:
+ *   dX = sum_i dY_i.W_i^T  (on-chip shard sum; written back in chunks)
+ *   dW_i = X^T.dY_i,  db = column sums of [dY_1 .. dY_t]
+ *   dY_shards [t] of [T, oi] bf16;  X, W_shards as in the forward
+ *   dX        [seq_chunks] chunks of [Tc, in] bf16 (output)
+ *   dW_shards [t] of [in, oi] fp32 (output, overwritten)
+ *   db        [out] fp32 (output, overwritten)
+ * With T = 0 the forward does nothing and the backward zeroes dW and db. */
+tpmlp_status tpmlp_column_linear_forward(const tpmlp_linear_dims* dims,
+                                         const void* const* X,
+                                         const void* const* W_shards, const void* b,
+                                         void* const* Y_shards,
+                                         void* workspace, void* stream);
+tpmlp_status tpmlp_column_linear_backward(const tpmlp_linear_dims* dims,
+                                          const void* const* dY_shards,
+                                          const void* const* X,
+                                          const void* const* W_shards,
+                                          void* const* dX,
+                                          void* const* dW_shards, void* db,
+                                          void* workspace, void* stream);
+
+/* Row-parallel forward:  Z = (sum_i X_i.W_i) + b   (b added once, after the
+ * shard sum -- the AllReduce of [CH2] 2.2 done on chip)
+ *   X_shards [t] of [T, ii] bf16 (column block i of the input)
+ *   W_shards [t] of [ii, out] bf16 (row block i of W)
+ *   b        [out] bf16
+ *   Z        [seq_chunks] chunks of [Tc, out] bf16 (output, reduce-scattered)
+ * Backward for upstream dZ:
+ *   dX_i = dZ.W_i^T,  dW_i = X_i^T.dZ,  db = column sums of dZ
+ *   dZ        [seq_chunks] chunks of [Tc, out] bf16;  X_shards, W_shards as in the forward
+ *   dX_shards [t] of [T, ii] bf16 (output)
+ *   dW_shards [t] of [ii, out] fp32 (output, overwritten)
+ *   db        [out] fp32 (output, overwritten)
+ * With T = 0 the forward does nothing and the backward zeroes dW and db. */
+tpmlp_status tpmlp_row_linear_forward(const tpmlp_linear_dims* dims,
+                                      const void* const* X_shards,
+                                      const void* const* W_shards, const void* b,
+                                      void* const* Z,
+                                      void* workspace, void* stream);
+tpmlp_status tpmlp_row_linear_backward(const tpmlp_linear_dims* dims,
+                                       const void* const* dZ,
+                                       const void* const* X_shards,
+                                       const void* const* W_shards,
+                                       void* const* dX_shards,
+                                       void* const* dW_shards, void* db,
+                                       void* workspace, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* tpmlp_status_string(tpmlp_status s);
 
@@ -241,8 +321,11 @@ enum {
     TPMLP_KERNEL_DGRAD_X = 3,     /* dX = sum_i dY_i.A_i^T */
     TPMLP_KERNEL_WGRAD_B = 4,     /* dB_i = H_i^T.dZ */
     TPMLP_KERNEL_WGRAD_A = 5,     /* dA_i = X^T.dY_i */
-    TPMLP_KERNEL_BIAS_GRAD = 6,   /* db1, db2 column sums (all launches) */
-    TPMLP_KERNEL_KINDS = 7
+    TPMLP_KERNEL_BIAS_GRAD = 6,   /* db1, db2, linear db column sums (all launches) */
+    TPMLP_KERNEL_LINEAR_FWD = 7,  /* linear layers: Y_i = X.W_i + b, Z = sum_i X_i.W_i + b */
+    TPMLP_KERNEL_LINEAR_DGRAD = 8,  /* linear layers: dX = sum_i dY_i.W_i^T, dX_i = dZ.W_i^T */
+    TPMLP_KERNEL_LINEAR_WGRAD = 9,  /* linear layers: dW_i */
+    TPMLP_KERNEL_KINDS = 10
 };
 tpmlp_status tpmlp_profile_begin(int capacity);
 int tpmlp_profile_end(double* ms, int* launches, int nkinds);

@@ -2,7 +2,7 @@
 
 Argument marshalling only: torch tensors become device pointers, lists become
 host pointer arrays, a non-OK status becomes a :class:`TpmlpError`.  Every step
-of the MLP block runs in the library's CUDA kernels.  There is no fallback: if
+of the MLP block and of the linear layers runs in the library's CUDA kernels.  There is no fallback: if
 the library has not been built, importing this module raises.
 """
 from __future__ import annotations
@@ -27,7 +27,7 @@ TPMLP_ERR_UNSUPPORTED = 2
 TPMLP_ERR_CUDA = 3
 TPMLP_ERR_TIMEOUT = 4
 
-KERNEL_KINDS = 7
+KERNEL_KINDS = 10
 
 # every symbol include/tpmlp.h declares
 EXPORTED = (
@@ -36,12 +36,20 @@ EXPORTED = (
     "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
     "tpmlp_kernel_name", "tpmlp_column_sums_noalloc", "tpmlp_set_split_min_kblocks",
     "tpmlp_recompute_workspace_bytes", "tpmlp_forward_recompute", "tpmlp_backward_recompute",
+    "tpmlp_linear_workspace_bytes", "tpmlp_column_linear_forward", "tpmlp_column_linear_backward",
+    "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
 )
 
 
 class tpmlp_dims(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("t", ctypes.c_int32), ("seq_chunks", ctypes.c_int32)]
+
+
+class tpmlp_linear_dims(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int64), ("in_features", ctypes.c_int64),
+                ("out_features", ctypes.c_int64), ("t", ctypes.c_int32),
+                ("seq_chunks", ctypes.c_int32)]
 
 
 class TpmlpError(RuntimeError):
@@ -54,6 +62,7 @@ _vp = ctypes.c_void_p
 _vpp = ctypes.POINTER(ctypes.c_void_p)
 _dims_p = ctypes.POINTER(tpmlp_dims)
 _sz_p = ctypes.POINTER(ctypes.c_size_t)
+_ldims_p = ctypes.POINTER(tpmlp_linear_dims)
 
 _lib.tpmlp_workspace_bytes.restype = ctypes.c_size_t
 _lib.tpmlp_workspace_bytes.argtypes = [_dims_p]
@@ -90,6 +99,14 @@ _lib.tpmlp_kernel_name.restype = ctypes.c_char_p
 _lib.tpmlp_kernel_name.argtypes = [ctypes.c_int]
 _lib.tpmlp_column_sums_noalloc.restype = ctypes.c_int
 _lib.tpmlp_column_sums_noalloc.argtypes = [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp]
+_lib.tpmlp_linear_workspace_bytes.restype = ctypes.c_size_t
+_lib.tpmlp_linear_workspace_bytes.argtypes = [_ldims_p]
+for _name in ("tpmlp_column_linear_forward", "tpmlp_row_linear_forward"):
+    getattr(_lib, _name).restype = ctypes.c_int
+    getattr(_lib, _name).argtypes = [_ldims_p, _vpp, _vpp, _vp, _vpp, _vp, _vp]
+for _name in ("tpmlp_column_linear_backward", "tpmlp_row_linear_backward"):
+    getattr(_lib, _name).restype = ctypes.c_int
+    getattr(_lib, _name).argtypes = [_ldims_p, _vpp, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _vp]
 
 
 def library_path() -> str:
@@ -102,6 +119,12 @@ def library():
 
 def make_dims(tokens: int, hidden: int, ffn: int, t: int, seq_chunks: int = 1) -> tpmlp_dims:
     return tpmlp_dims(int(tokens), int(hidden), int(ffn), int(t), int(seq_chunks))
+
+
+def make_linear_dims(tokens: int, in_features: int, out_features: int, t: int,
+                     seq_chunks: int = 1) -> tpmlp_linear_dims:
+    return tpmlp_linear_dims(int(tokens), int(in_features), int(out_features), int(t),
+                             int(seq_chunks))
 
 
 def _ptr(x) -> int | None:
@@ -226,3 +249,38 @@ def tpmlp_column_sums_noalloc(src, rows: int, cols: int, out, stream=None) -> in
     allocation (library-owned static scratch).  Returns the status."""
     return int(_lib.tpmlp_column_sums_noalloc(_ptr(src), int(rows), int(cols), _ptr(out),
                                               _stream(stream)))
+
+
+def tpmlp_linear_workspace_bytes(dims: tpmlp_linear_dims) -> int:
+    """Scratch bytes of any linear-layer call with these dims (0 if invalid)."""
+    return int(_lib.tpmlp_linear_workspace_bytes(ctypes.byref(dims)))
+
+
+def tpmlp_column_linear_forward(dims, X, W_shards, b, Y_shards, workspace, stream=None) -> None:
+    """X: seq_chunks tensors [Tc, in]; W_shards, Y_shards: t tensors."""
+    _check(_lib.tpmlp_column_linear_forward(ctypes.byref(dims), _arr(X), _arr(W_shards), _ptr(b),
+                                            _arr(Y_shards), _ptr(workspace), _stream(stream)),
+           "tpmlp_column_linear_forward")
+
+
+def tpmlp_column_linear_backward(dims, dY_shards, X, W_shards, dX, dW_shards, db, workspace,
+                                 stream=None) -> None:
+    _check(_lib.tpmlp_column_linear_backward(ctypes.byref(dims), _arr(dY_shards), _arr(X),
+                                             _arr(W_shards), _arr(dX), _arr(dW_shards), _ptr(db),
+                                             _ptr(workspace), _stream(stream)),
+           "tpmlp_column_linear_backward")
+
+
+def tpmlp_row_linear_forward(dims, X_shards, W_shards, b, Z, workspace, stream=None) -> None:
+    """X_shards, W_shards: t tensors; Z: seq_chunks tensors [Tc, out]."""
+    _check(_lib.tpmlp_row_linear_forward(ctypes.byref(dims), _arr(X_shards), _arr(W_shards),
+                                         _ptr(b), _arr(Z), _ptr(workspace), _stream(stream)),
+           "tpmlp_row_linear_forward")
+
+
+def tpmlp_row_linear_backward(dims, dZ, X_shards, W_shards, dX_shards, dW_shards, db, workspace,
+                              stream=None) -> None:
+    _check(_lib.tpmlp_row_linear_backward(ctypes.byref(dims), _arr(dZ), _arr(X_shards),
+                                          _arr(W_shards), _arr(dX_shards), _arr(dW_shards),
+                                          _ptr(db), _ptr(workspace), _stream(stream)),
+           "tpmlp_row_linear_backward")

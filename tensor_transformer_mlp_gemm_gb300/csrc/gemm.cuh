@@ -283,8 +283,8 @@ template <int EPI>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int part, long long row,
                                               int m, int n, float (&x)[32], float (&x2)[32]) {
     if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS) {
-        const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(p.bias) + n +
-                                 (EPI == EPI_BIAS_GELU ? g * p.bias_group_stride : 0);
+        const __nv_bfloat16* b =
+            static_cast<const __nv_bfloat16*>(p.bias) + n + g * p.bias_group_stride;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (n + 8 * q < p.N) {

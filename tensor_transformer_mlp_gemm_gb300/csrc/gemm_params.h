@@ -87,7 +87,7 @@ struct GemmParams {
     long long ld_in;         // leading dimension of in0 (elements)
     int out_part;            // PART_GROUP or PART_ROW
     int out_rows_per_part;   // rows per output chunk for PART_ROW
-    int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU)
+    int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU, EPI_BIAS)
     // control
     unsigned int* err;
     unsigned long long timeout_ns;
@@ -98,10 +98,10 @@ struct GemmParams {
 // persistent grid of CTA pairs (at most one pair per tile, at most as many
 // pairs as fit on the GPU at once).
 //   column_fwd : A K-major,  B MN-major, EPI_BIAS_GELU  (Y_i, H_i)
-//   row_fwd    : A K-major,  B MN-major, EPI_BIAS       (Z)
+//   row_fwd    : A K-major,  B MN-major, EPI_BIAS       (Z; column-linear Y_i)
 //   dgrad_h    : A K-major,  B K-major,  EPI_DGELU      (dY_i)
-//   dgrad_x    : A K-major,  B K-major,  EPI_BF16       (dX)
-//   wgrad      : A MN-major, B MN-major, EPI_F32        (dA_i, dB_i)
+//   dgrad_x    : A K-major,  B K-major,  EPI_BF16       (dX; row-linear dX_i)
+//   wgrad      : A MN-major, B MN-major, EPI_F32        (dA_i, dB_i; linear dW_i)
 cudaError_t launch_column_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_row_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_dgrad_h(const GemmParams& p, cudaStream_t stream);

@@ -30,9 +30,10 @@
 #include <mutex>
 #include <vector>
 
-#include "tpmlp.h"
+#include "abi_internal.h"
 #include "colsum.cuh"
 #include "gemm_params.h"
+#include "tpmlp.h"
 
 #define TPMLP_API extern "C" __attribute__((visibility("default")))
 
@@ -41,18 +42,11 @@ namespace tpmlp {
 // Device error word: kernels OR a bit in when a bounded wait expires.
 __device__ unsigned int g_error_word;
 
+namespace abi {
+
 namespace {
-
 constexpr int kMaxDevices = 64;
-constexpr int kMaxShards = 8;
-constexpr int kBand = 8;   // cluster M-tiles (256 rows each) per raster band
-
-struct DeviceInfo {
-    bool ready = false;
-    bool supported = false;
-    int sm_count = 0;
-    unsigned int* err = nullptr;
-};
+}  // namespace
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
@@ -66,11 +60,6 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn g_encode = nullptr;
 
 // ---- profiling ------------------------------------------------------------------
-struct ProfRec {
-    int kind;
-    int kernels;  // kernel launches between the two events
-    cudaEvent_t a, b;
-};
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof_pool;
@@ -83,15 +72,6 @@ ProfRec* prof_next(int kind, int kernels) {
     r->kind = kind;
     r->kernels = kernels;
     return r;
-}
-
-template <typename F>
-cudaError_t timed(int kind, int kernels, cudaStream_t s, F&& launch) {
-    ProfRec* r = prof_next(kind, kernels);
-    if (r) cudaEventRecord(r->a, s);
-    cudaError_t e = launch();
-    if (r) cudaEventRecord(r->b, s);
-    return e;
 }
 
 // ---- device / driver ----------------------------------------------------------------
@@ -132,7 +112,7 @@ tpmlp_status device_info(DeviceInfo** out) {
 // bf16 row-major matrix [outer, inner] with leading dimension ld (elements).
 //   K-major operand tile: box {BK, box_rows} (BK along the contiguous K axis)
 //   MN-major operand tile: box {64, BK}      (64 along the contiguous M/N axis)
-bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
+static bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld,
                  uint32_t box_inner, uint32_t box_outer) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {ld * 2};
@@ -168,45 +148,6 @@ bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, b
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// ---- workspace ---------------------------------------------------------------------------
-inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-struct Layout {
-    size_t y, h, dy, part1, part2, split_part, split_cnt, total;
-};
-
-Layout layout_of(const tpmlp_dims& d) {
-    Layout L;
-    const size_t act = align256(static_cast<size_t>(d.tokens) * static_cast<size_t>(d.ffn) * 2);
-    L.y = 0;
-    L.h = act;
-    L.dy = 2 * act;
-    L.part1 = 3 * act;
-    L.part2 = L.part1 + align256(colsum_scratch_bytes(d.ffn));
-    L.split_part = L.part2 + align256(colsum_scratch_bytes(d.hidden));
-    L.split_cnt = L.split_part + align256(static_cast<size_t>(MAX_SPLIT_UNITS) * CLUSTER_M * BN * 4);
-    L.total = L.split_cnt + align256(static_cast<size_t>(MAX_SPLIT_UNITS) * 2 * sizeof(int));
-    return L;
-}
-
-// ---- validation --------------------------------------------------------------------------
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-tpmlp_status check_dims(const tpmlp_dims* d) {
-    if (!d) return TPMLP_ERR_INVALID_ARG;
-    if (d->tokens < 0 || d->hidden <= 0 || d->ffn <= 0 || d->t <= 0 || d->seq_chunks <= 0)
-        return TPMLP_ERR_INVALID_ARG;
-    if (d->ffn % d->t != 0) return TPMLP_ERR_INVALID_ARG;
-    if (d->tokens % d->seq_chunks != 0) return TPMLP_ERR_INVALID_ARG;
-    if (d->t > kMaxShards || d->seq_chunks > kMaxShards) return TPMLP_ERR_UNSUPPORTED;
-    const int64_t fi = d->ffn / d->t;
-    if (d->hidden % 8 != 0 || fi % 8 != 0) return TPMLP_ERR_UNSUPPORTED;
-    const int64_t lim = (int64_t(1) << 31) - 1;
-    if (d->tokens > lim || d->hidden > lim || d->ffn > lim) return TPMLP_ERR_UNSUPPORTED;
-    if (d->seq_chunks > 1 && (d->tokens / d->seq_chunks) % BM != 0) return TPMLP_ERR_UNSUPPORTED;
-    return TPMLP_OK;
-}
-
 tpmlp_status check_ptrs(const void* const* arr, int n) {
     if (!arr) return TPMLP_ERR_INVALID_ARG;
     for (int i = 0; i < n; ++i) {
@@ -220,17 +161,6 @@ tpmlp_status check_ptr(const void* p) {
     if (!p) return TPMLP_ERR_INVALID_ARG;
     return aligned16(p) ? TPMLP_OK : TPMLP_ERR_UNSUPPORTED;
 }
-
-#define TPMLP_TRY(expr)                        \
-    do {                                       \
-        tpmlp_status _s = (expr);              \
-        if (_s != TPMLP_OK) return _s;         \
-    } while (0)
-
-#define TPMLP_CUDA(expr)                                \
-    do {                                                \
-        if ((expr) != cudaSuccess) return TPMLP_ERR_CUDA; \
-    } while (0)
 
 // ---- GEMM set-up ------------------------------------------------------------------------
 void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int groups,
@@ -254,6 +184,62 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     p.bias_group_stride = 0;
     p.ld_in = 0;
     for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
+}
+
+bool attach_split(GemmParams& p, void* split_part, void* split_cnt) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(BN),
+                          static_cast<cuuint64_t>(MAX_SPLIT_UNITS) * CLUSTER_M};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(BN) * 4};
+    cuuint32_t box[2] = {EPI_CHUNK, 32};
+    cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, split_part, dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    p.partial = reinterpret_cast<const float*>(split_part);
+    p.counters = reinterpret_cast<int*>(split_cnt);
+    p.split_min_kblocks = g_split_min_kblocks;
+    return true;
+}
+
+}  // namespace abi
+
+namespace {
+
+using namespace abi;
+
+// ---- workspace ---------------------------------------------------------------------------
+struct Layout {
+    size_t y, h, dy, part1, part2, split_part, split_cnt, total;
+};
+
+Layout layout_of(const tpmlp_dims& d) {
+    Layout L;
+    const size_t act = align256(static_cast<size_t>(d.tokens) * static_cast<size_t>(d.ffn) * 2);
+    L.y = 0;
+    L.h = act;
+    L.dy = 2 * act;
+    L.part1 = 3 * act;
+    L.part2 = L.part1 + align256(colsum_scratch_bytes(d.ffn));
+    L.split_part = L.part2 + align256(colsum_scratch_bytes(d.hidden));
+    L.split_cnt = L.split_part + split_part_bytes();
+    L.total = L.split_cnt + split_cnt_bytes();
+    return L;
+}
+
+tpmlp_status check_dims(const tpmlp_dims* d) {
+    if (!d) return TPMLP_ERR_INVALID_ARG;
+    if (d->tokens < 0 || d->hidden <= 0 || d->ffn <= 0 || d->t <= 0 || d->seq_chunks <= 0)
+        return TPMLP_ERR_INVALID_ARG;
+    if (d->ffn % d->t != 0) return TPMLP_ERR_INVALID_ARG;
+    if (d->tokens % d->seq_chunks != 0) return TPMLP_ERR_INVALID_ARG;
+    if (d->t > kMaxShards || d->seq_chunks > kMaxShards) return TPMLP_ERR_UNSUPPORTED;
+    const int64_t fi = d->ffn / d->t;
+    if (d->hidden % 8 != 0 || fi % 8 != 0) return TPMLP_ERR_UNSUPPORTED;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (d->tokens > lim || d->hidden > lim || d->ffn > lim) return TPMLP_ERR_UNSUPPORTED;
+    if (d->seq_chunks > 1 && (d->tokens / d->seq_chunks) % BM != 0) return TPMLP_ERR_UNSUPPORTED;
+    return TPMLP_OK;
 }
 
 // Device buffers one forward/backward pair works in.  The standard calls
@@ -286,21 +272,8 @@ Regions recompute_regions(uint8_t* saved, uint8_t* scratch, const Layout& L) {
                    scratch + (L.split_cnt - L.h)};
 }
 
-// Workspace buffers of the tail split (see gemm_params.h).
 bool attach_split(GemmParams& p, const Regions& R) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(BN),
-                          static_cast<cuuint64_t>(MAX_SPLIT_UNITS) * CLUSTER_M};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(BN) * 4};
-    cuuint32_t box[2] = {EPI_CHUNK, 32};
-    cuuint32_t estr[2] = {1, 1};
-    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, R.split_part, dims,
-                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    p.partial = reinterpret_cast<const float*>(R.split_part);
-    p.counters = reinterpret_cast<int*>(R.split_cnt);
-    p.split_min_kblocks = g_split_min_kblocks;
-    return true;
+    return abi::attach_split(p, R.split_part, R.split_cnt);
 }
 
 struct Shapes {
@@ -545,6 +518,7 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
 }  // namespace tpmlp
 
 using namespace tpmlp;
+using namespace tpmlp::abi;
 
 // =========================================================================================
 TPMLP_API const char* tpmlp_status_string(tpmlp_status s) {
@@ -809,6 +783,9 @@ TPMLP_API const char* tpmlp_kernel_name(int kind) {
         case TPMLP_KERNEL_WGRAD_B: return "wgrad_b";
         case TPMLP_KERNEL_WGRAD_A: return "wgrad_a";
         case TPMLP_KERNEL_BIAS_GRAD: return "bias_grad";
+        case TPMLP_KERNEL_LINEAR_FWD: return "linear_fwd";
+        case TPMLP_KERNEL_LINEAR_DGRAD: return "linear_dgrad";
+        case TPMLP_KERNEL_LINEAR_WGRAD: return "linear_wgrad";
     }
     return "unknown";
 }

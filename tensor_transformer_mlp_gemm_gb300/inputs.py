@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the tensor-parallel MLP block.
+"""Seeded synthetic inputs for the tensor-parallel MLP block and the
+tensor-parallel linear layers (the attention projections).
 
 This module is shared by the CUDA path's tests/benchmark and by the oracle's
 tests.  It draws random numbers and lays them out (shards, sequence chunks);
@@ -9,6 +10,10 @@ in this order, X [T, h], A [h, f], b1 [f], B [f, h], b2 [h], dZ [T, h] with
 ``torch.randn`` in fp32; each draw is multiplied by its standard deviation and
 rounded to bf16 (round to nearest even).  X and dZ have std 1, the weights
 ``sigma_w``, the biases 0.02.
+
+Linear layers (``make_linear_inputs``): the same kind of generator draws, in
+this order, X [T, in], W [in, out], b [out], dY [T, out] (dY is the upstream
+gradient of the layer's output), with the same standard deviations.
 
 Token rows are ordered sequence-major ([seq, micro-batch] flattened, the usual
 [s, b, h] activation layout), so sequence chunk j is the contiguous row range
@@ -111,3 +116,71 @@ def seq_chunks(X: torch.Tensor, n: int) -> list:
         raise ValueError("T must be divisible by the number of chunks")
     r = T // n
     return [X[j * r:(j + 1) * r, :].contiguous() for j in range(n)]
+
+
+@dataclass(frozen=True)
+class LinearWorkload:
+    """One tensor-parallel linear layer: W [in, out] split by columns
+    (split="column": Y_i = X.W_i + b_i) or by rows (split="row":
+    Z = sum_i X_i.W_i + b)."""
+    name: str
+    tokens: int
+    in_features: int
+    out_features: int
+    t: int
+    split: str            # "column" or "row"
+    sigma_w: float
+    seq_chunks: int = 1
+    sigma_b: float = 0.02
+
+    @property
+    def flops(self) -> int:
+        """fwd+bwd FLOPs: three GEMMs (forward, input gradient, weight gradient)
+        of 2*T*in*out each."""
+        return 6 * self.tokens * self.in_features * self.out_features
+
+    @property
+    def shard(self) -> int:
+        """out / t (column split) or in / t (row split)."""
+        return (self.out_features if self.split == "column" else self.in_features) // self.t
+
+
+# Attention projections of the pages' 175B-class layer: hidden 12288, the QKV
+# weight 12288 x 36864 split 8 ways into 12288 x 4608 (column parallel), the
+# output projection 12288 x 12288 split 8 ways by rows; 2048 tokens as in the
+# MLP workload.  Plus small cases.
+LINEAR_WORKLOADS = {
+    "qkv_tiny": LinearWorkload("qkv_tiny", 128, 256, 768, 2, "column", 0.02),
+    "attn_out_tiny": LinearWorkload("attn_out_tiny", 128, 256, 256, 2, "row", 0.02),
+    "qkv_175b": LinearWorkload("qkv_175b", 2048, 12288, 36864, 8, "column", 0.006),
+    "attn_out_175b": LinearWorkload("attn_out_175b", 2048, 12288, 12288, 8, "row", 0.006),
+    "qkv_sp_h4096": LinearWorkload("qkv_sp_h4096", 16384, 4096, 12288, 8, "column", 0.02,
+                                   seq_chunks=8),
+    "attn_out_sp_h4096": LinearWorkload("attn_out_sp_h4096", 16384, 4096, 4096, 8, "row", 0.02,
+                                        seq_chunks=8),
+}
+
+
+def custom_linear(tokens: int, in_features: int, out_features: int, t: int, split: str,
+                  sigma_w: float = 0.02, seq_chunks: int = 1,
+                  name: str = "custom_linear") -> LinearWorkload:
+    return LinearWorkload(name, tokens, in_features, out_features, t, split, sigma_w, seq_chunks)
+
+
+def make_linear_inputs(w: LinearWorkload, seed: int = 0) -> dict:
+    """Full (unsharded) bf16 CPU tensors X [T, in], W [in, out], b [out],
+    dY [T, out] for linear workload w."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+
+    def draw(shape, std):
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(torch.bfloat16)
+
+    X = draw((w.tokens, w.in_features), 1.0)
+    W = draw((w.in_features, w.out_features), w.sigma_w)
+    b = draw((w.out_features,), w.sigma_b)
+    dY = draw((w.tokens, w.out_features), 1.0)
+    return {"X": X, "W": W, "b": b, "dY": dY}

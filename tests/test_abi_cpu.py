@@ -53,7 +53,8 @@ def test_status_strings(binding):
         assert binding.tpmlp_status_string(s)
     assert binding.tpmlp_status_string(99) == "unknown status"
     assert [binding.tpmlp_kernel_name(k) for k in range(binding.KERNEL_KINDS)] == [
-        "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad"]
+        "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad",
+        "linear_fwd", "linear_dgrad", "linear_wgrad"]
 
 
 def test_workspace_bytes(binding):
@@ -135,6 +136,56 @@ def test_recompute_workspace_and_validation(binding):
     assert lib.tpmlp_backward_recompute(ctypes.byref(d), arr(one), arr(one), arr(two), arr(two),
                                         FAKE, FAKE + 8, arr(one), arr(two), FAKE, arr(two), FAKE,
                                         None) == binding.TPMLP_ERR_UNSUPPORTED  # misaligned
+
+
+def test_linear_workspace_bytes(binding):
+    mk = binding.make_linear_dims
+    n = binding.tpmlp_linear_workspace_bytes(mk(2048, 12288, 36864, 8))
+    assert n >= 64 * 36864 * 4 + 128 * 256 * 256 * 4   # bias partials + split tiles
+    assert binding.tpmlp_linear_workspace_bytes(mk(128, 256, 264, 2)) > 0   # valid as a row split
+    assert binding.tpmlp_linear_workspace_bytes(mk(128, 100, 256, 2)) == 0  # valid as neither
+    assert binding.tpmlp_linear_workspace_bytes(mk(0, 64, 64, 1)) > 0
+
+
+def _lin(binding, fn, dims, nin=None, W=None, b=FAKE, nout=None, ws=FAKE):
+    lib = binding.library()
+    arr = lambda xs: (ctypes.c_void_p * max(len(xs), 1))(*xs)
+    W = W if W is not None else [FAKE] * dims.t
+    if fn in ("tpmlp_column_linear_forward", "tpmlp_row_linear_forward"):
+        col = fn.startswith("tpmlp_column")
+        ins = nin if nin is not None else [FAKE] * (dims.seq_chunks if col else dims.t)
+        outs = nout if nout is not None else [FAKE] * (dims.t if col else dims.seq_chunks)
+        return getattr(lib, fn)(ctypes.byref(dims), arr(ins), arr(W), b, arr(outs), ws, None)
+    n = max(dims.t, dims.seq_chunks)
+    ins = nin if nin is not None else [FAKE] * n
+    outs = nout if nout is not None else [FAKE] * n
+    return getattr(lib, fn)(ctypes.byref(dims), arr(ins), arr([FAKE] * n), arr(W), arr(outs),
+                            arr([FAKE] * dims.t), b, ws, None)
+
+
+def test_linear_validation_codes(binding):
+    mk = binding.make_linear_dims
+    INV, UNS = binding.TPMLP_ERR_INVALID_ARG, binding.TPMLP_ERR_UNSUPPORTED
+    colf, rowf = "tpmlp_column_linear_forward", "tpmlp_row_linear_forward"
+    colb, rowb = "tpmlp_column_linear_backward", "tpmlp_row_linear_backward"
+    for fn in (colf, colb, rowf, rowb):
+        assert _lin(binding, fn, mk(-1, 256, 256, 2)) == INV             # negative tokens
+        assert _lin(binding, fn, mk(256, 256, 256, 0)) == INV            # no shards
+        assert _lin(binding, fn, mk(256, 256, 256, 16)) == UNS           # more than 8 shards
+        assert _lin(binding, fn, mk(384, 256, 256, 2, 2)) == UNS         # chunk of 192 rows
+        assert _lin(binding, fn, mk(256, 256, 256, 2), ws=None) == INV   # no workspace
+        assert _lin(binding, fn, mk(256, 256, 256, 2), b=FAKE + 4) == UNS
+        assert _lin(binding, fn, mk(256, 256, 256, 2), W=[FAKE, None]) == INV
+    assert _lin(binding, colf, mk(256, 256, 300, 7)) == INV   # t does not divide out
+    assert _lin(binding, colf, mk(256, 300, 256, 2)) == UNS   # in not a multiple of 8
+    assert _lin(binding, colf, mk(256, 256, 260, 2)) == UNS   # oi = 130 not a multiple of 8
+    assert _lin(binding, rowf, mk(256, 300, 256, 7)) == INV   # t does not divide in
+    assert _lin(binding, rowf, mk(256, 260, 256, 2)) == UNS   # ii = 130
+    assert _lin(binding, rowf, mk(256, 256, 300, 2)) == UNS   # out not a multiple of 8
+    assert _lin(binding, colf, mk(256, 256, 256, 2), nout=[FAKE, FAKE + 2]) == UNS
+    assert _lin(binding, rowf, mk(256, 256, 256, 2), nin=[None, FAKE]) == INV
+    assert binding.library().tpmlp_row_linear_forward(None, None, None, None, None, None,
+                                                      None) == INV
 
 
 def test_set_timeout_and_profile_args(binding):
