@@ -196,27 +196,39 @@ __device__ __forceinline__ void epilogue_bar() {
 // CTA of a pair tile when T is not a multiple of 256) reads the last chunk's
 // map at out-of-range rows, which TMA fills with zeros; the map index never
 // leaves the encoded maps.
-template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand(const CUtensorMap* maps, int part, int rows_per_map,
-                                             int nmaps, int g, int s, int row0, int kc, int K,
-                                             uint32_t dst, uint32_t bar) {
-    int idx = 0, r = row0, k = s * K + kc;
+struct OperandCursor {
+    const CUtensorMap* map;
+    int r;      // row (M or N) coordinate of this CTA's box
+    int kbase;  // K coordinate of the segment's first element
+};
+
+__device__ __forceinline__ OperandCursor operand_cursor(const CUtensorMap* maps, int part,
+                                                        int rows_per_map, int nmaps, int g,
+                                                        int s, int row0, int K) {
+    OperandCursor c{maps, row0, s * K};
     if (part == PART_GROUP) {
-        idx = g;
+        c.map = maps + g;
     } else if (part == PART_KSEG) {
-        idx = s;
-        k = kc;
+        c.map = maps + s;
+        c.kbase = 0;
     } else if (part == PART_ROW) {
-        idx = min(row0 / rows_per_map, nmaps - 1);
-        r = row0 - idx * rows_per_map;
+        const int idx = min(row0 / rows_per_map, nmaps - 1);
+        c.map = maps + idx;
+        c.r = row0 - idx * rows_per_map;
     }
-    const CUtensorMap* m = maps + idx;
+    return c;
+}
+
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(const OperandCursor& c, int kc, uint32_t dst,
+                                             uint32_t bar) {
+    const int k = c.kbase + kc;
     if constexpr (!MN) {
-        ptx::tma_load_2d_pair(dst, m, k, r, bar);
+        ptx::tma_load_2d_pair(dst, c.map, k, c.r, bar);
     } else {
 #pragma unroll
         for (int j = 0; j < ROWS / MN_CHUNK; ++j)
-            ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, m, r + j * MN_CHUNK, k, bar);
+            ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, c.map, c.r + j * MN_CHUNK, k, bar);
     }
 }
 
@@ -391,9 +403,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 decode_tile(p, it.tile, g, m0, n0);
                 const int a_row = m0 + rank * BM;
                 const int b_row = n0 + rank * B_ROWS;
+                // segment and K step advance by increments; the map and row of each
+                // operand change only with the segment
+                int seg = it.kbeg / kblocks;
+                int kb = it.kbeg - seg * kblocks;
+                OperandCursor ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps,
+                                                  g, seg, a_row, p.K);
+                OperandCursor cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps,
+                                                  g, seg, b_row, p.K);
                 for (int kk = it.kbeg; kk < it.kend; ++kk) {
-                    const int s = kk / kblocks;
-                    const int kb = kk - s * kblocks;
+                    if (kb == kblocks) {
+                        kb = 0;
+                        ++seg;
+                        ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps, g,
+                                            seg, a_row, p.K);
+                        cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g,
+                                            seg, b_row, p.K);
+                    }
                     {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
                                           ERR_PRODUCER)) {
@@ -405,11 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             const uint32_t sa = base + stage * STAGE_BYTES;
                             if (rank == 0)  // counts both CTAs' bytes
                                 ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * STAGE_BYTES);
-                            load_operand<A_MN, BM>(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps,
-                                                   g, s, a_row, kb * BK, p.K, sa, full);
-                            load_operand<B_MN, B_ROWS>(p.b_map, p.b_part, p.b_rows_per_map,
-                                                       p.b_nmaps, g, s, b_row, kb * BK, p.K,
-                                                       sa + A_STAGE_BYTES, full);
+                            load_operand<A_MN, BM>(ca, kb * BK, sa, full);
+                            load_operand<B_MN, B_ROWS>(cb, kb * BK, sa + A_STAGE_BYTES, full);
                             ++fills;
                         }
                         if (++stage == STAGES) {
@@ -417,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             phase ^= 1u;
                         }
                     }
+                    ++kb;
                 }
             }
             if (ok) {
