@@ -35,7 +35,9 @@ tpmlp_status device_info(DeviceInfo** out);
 //   MN-major operand [K, rows]: box {64, BK}
 //   output [rows, cols], bf16 or fp32: box 32 x 32 for the epilogue's stores
 bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, int box_rows);
-bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K);
+// MN-major maps are 3-D {64, K, rows / 64} when rows is a multiple of 64 (one
+// copy per box), else 2-D; *mn3d (the operand's GemmParams flag) says which.
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d);
 bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, bool f32);
 
 // ---- workspace pieces ------------------------------------------------------------------

@@ -200,12 +200,13 @@ struct OperandCursor {
     const CUtensorMap* map;
     int r;      // row (M or N) coordinate of this CTA's box
     int kbase;  // K coordinate of the segment's first element
+    int mn3d;   // MN-major operand encoded as a 3-D map {64, K, rows / 64}
 };
 
 __device__ __forceinline__ OperandCursor operand_cursor(const CUtensorMap* maps, int part,
                                                         int rows_per_map, int nmaps, int g,
-                                                        int s, int row0, int K) {
-    OperandCursor c{maps, row0, s * K};
+                                                        int s, int row0, int K, int mn3d) {
+    OperandCursor c{maps, row0, s * K, mn3d};
     if (part == PART_GROUP) {
         c.map = maps + g;
     } else if (part == PART_KSEG) {
@@ -226,9 +227,14 @@ __device__ __forceinline__ void load_operand(const OperandCursor& c, int kc, uin
     if constexpr (!MN) {
         ptx::tma_load_2d_pair(dst, c.map, k, c.r, bar);
     } else {
+        if (c.mn3d) {
+            // box {64, BK, ROWS / 64}: chunk j lands at dst + j * MN_CHUNK_BYTES
+            ptx::tma_load_3d_pair(dst, c.map, 0, k, c.r / MN_CHUNK, bar);
+        } else {
 #pragma unroll
-        for (int j = 0; j < ROWS / MN_CHUNK; ++j)
-            ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, c.map, c.r + j * MN_CHUNK, k, bar);
+            for (int j = 0; j < ROWS / MN_CHUNK; ++j)
+                ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, c.map, c.r + j * MN_CHUNK, k, bar);
+        }
     }
 }
 
@@ -408,17 +414,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 int seg = it.kbeg / kblocks;
                 int kb = it.kbeg - seg * kblocks;
                 OperandCursor ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps,
-                                                  g, seg, a_row, p.K);
+                                                  g, seg, a_row, p.K, p.a_mn3d);
                 OperandCursor cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps,
-                                                  g, seg, b_row, p.K);
+                                                  g, seg, b_row, p.K, p.b_mn3d);
                 for (int kk = it.kbeg; kk < it.kend; ++kk) {
                     if (kb == kblocks) {
                         kb = 0;
                         ++seg;
                         ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps, g,
-                                            seg, a_row, p.K);
+                                            seg, a_row, p.K, p.a_mn3d);
                         cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g,
-                                            seg, b_row, p.K);
+                                            seg, b_row, p.K, p.b_mn3d);
                     }
                     {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,

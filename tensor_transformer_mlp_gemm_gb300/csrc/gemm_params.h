@@ -70,6 +70,9 @@ struct GemmParams {
     int a_part, b_part;
     int a_rows_per_map, b_rows_per_map;
     int a_nmaps, b_nmaps;   // encoded maps; PART_ROW indices are clamped to them
+    // MN-major operands whose row count is a multiple of 64 are encoded as 3-D
+    // maps {64, K, rows / 64} so one copy fetches every 64-row chunk of a box
+    int a_mn3d, b_mn3d;
     // tail split (set by the launcher; units = 0 means every tile is whole)
     int dp_tiles;           // tiles computed whole, in schedule order 0..dp_tiles-1
     int splits;             // K splits per leftover tile

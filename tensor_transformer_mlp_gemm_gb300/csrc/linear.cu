@@ -134,7 +134,7 @@ tpmlp_status column_forward(const Lin& s, const DeviceInfo* dev, const void* con
     p.a_nmaps = s.chunks;
     p.a_rows_per_map = s.Tc;
     for (int i = 0; i < s.t; ++i)
-        if (!encode_mnmajor(&p.b_map[i], W[i], s.shard, s.in)) return TPMLP_ERR_UNSUPPORTED;
+        if (!encode_mnmajor(&p.b_map[i], W[i], s.shard, s.in, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
     p.b_part = PART_GROUP;
     p.b_nmaps = s.t;
     for (int i = 0; i < s.t; ++i)
@@ -173,11 +173,11 @@ tpmlp_status column_backward(const Lin& s, const DeviceInfo* dev, const void* co
         GemmParams p;
         base_params(p, *dev, s.in, s.shard, s.Tc, s.t, s.chunks);
         for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.a_map[j], X[j], s.in, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.a_map[j], X[j], s.in, s.Tc, &p.a_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_KSEG;
         p.a_nmaps = s.chunks;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], dY[i], s.shard, s.T)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], dY[i], s.shard, s.T, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_nmaps = s.t;
         for (int i = 0; i < s.t; ++i)
@@ -200,7 +200,7 @@ tpmlp_status row_forward(const Lin& s, const DeviceInfo* dev, const void* const*
     base_params(p, *dev, s.T, s.out, s.shard, 1, s.t);
     for (int i = 0; i < s.t; ++i) {
         if (!encode_kmajor(&p.a_map[i], X[i], s.shard, s.T, BM)) return TPMLP_ERR_UNSUPPORTED;
-        if (!encode_mnmajor(&p.b_map[i], W[i], s.out, s.shard)) return TPMLP_ERR_UNSUPPORTED;
+        if (!encode_mnmajor(&p.b_map[i], W[i], s.out, s.shard, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
     }
     p.a_part = p.b_part = PART_KSEG;
     p.a_nmaps = p.b_nmaps = s.t;
@@ -242,11 +242,11 @@ tpmlp_status row_backward(const Lin& s, const DeviceInfo* dev, const void* const
         GemmParams p;
         base_params(p, *dev, s.shard, s.out, s.Tc, s.t, s.chunks);
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.a_map[i], X[i], s.shard, s.T)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.a_map[i], X[i], s.shard, s.T, &p.a_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_GROUP;
         p.a_nmaps = s.t;
         for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.out, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.out, s.Tc, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_KSEG;
         p.b_nmaps = s.chunks;
         for (int i = 0; i < s.t; ++i)

@@ -128,8 +128,24 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, i
     return encode_bf16(m, ptr, K, rows, K, BK, static_cast<uint32_t>(box_rows));
 }
 
-bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K) {
-    return encode_bf16(m, ptr, rows, K, rows, MN_CHUNK, BK);
+static_assert(BM == B_ROWS, "one 3-D MN-major box height serves both operands");
+
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d) {
+    if (rows % MN_CHUNK != 0) {
+        *mn3d = 0;
+        return encode_bf16(m, ptr, rows, K, rows, MN_CHUNK, BK);
+    }
+    // {64 elements, K rows, rows / 64 chunks}: chunk j starts 128 bytes after
+    // chunk j - 1, so a box {64, BK, 2} is two neighbouring 64-element columns
+    *mn3d = 1;
+    cuuint64_t dims[3] = {MN_CHUNK, K, rows / MN_CHUNK};
+    cuuint64_t strides[2] = {rows * 2, MN_CHUNK * 2};
+    cuuint32_t box[3] = {MN_CHUNK, BK, static_cast<cuuint32_t>(BM / MN_CHUNK)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Epilogue store map: row-major [rows, cols] output, box 32 x 32; fp32 boxes
@@ -329,7 +345,7 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
         p.b_nmaps = s.t;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
@@ -352,7 +368,7 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
         for (int i = 0; i < s.t; ++i) {
             if (!encode_kmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, BM))
                 return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = PART_KSEG;
         p.a_nmaps = s.t;
@@ -442,13 +458,13 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
         GemmParams p;
         base_params(p, *dev, s.fi, s.h, s.Tc, s.t, s.chunks);
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T))
+            if (!encode_mnmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, &p.a_mn3d))
                 return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_GROUP;
         p.a_nmaps = s.t;
         p.b_nmaps = s.chunks;
         for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[j], dZ[j], s.h, s.Tc, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_KSEG;
         p.a_rows_per_map = p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i)
@@ -465,12 +481,12 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
         GemmParams p;
         base_params(p, *dev, s.h, s.fi, s.Tc, s.t, s.chunks);
         for (int j = 0; j < s.chunks; ++j)
-            if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.a_map[j], X[j], s.h, s.Tc, &p.a_mn3d)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_KSEG;
         p.a_nmaps = s.chunks;
         p.b_nmaps = s.t;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T))
+            if (!encode_mnmajor(&p.b_map[i], shard_ptr(dY, i, s), s.fi, s.T, &p.b_mn3d))
                 return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.a_rows_per_map = p.b_rows_per_map = 0;
