@@ -1,5 +1,6 @@
-"""fp64 CPU oracle for the tensor-parallel Transformer MLP block and the
-column- and row-parallel linear layers it is built from.
+"""fp64 CPU oracle for the tensor-parallel Transformer MLP block, the
+column- and row-parallel linear layers it is built from, and the
+sequence-parallel LayerNorm / Dropout sublayer around it.
 
 TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product path
@@ -68,6 +69,13 @@ def _configure(lib):
     lib.oracle_column_linear_backward.argtypes = dims + [_dp, _dpp, _dpp, _dp, _dpp, _dp]
     lib.oracle_row_linear_forward.argtypes = dims + [_dpp, _dpp, _dp, _dp]
     lib.oracle_row_linear_backward.argtypes = dims + [_dpp, _dpp, _dp, _dpp, _dpp, _dp]
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    lib.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+    lib.oracle_dropout_keep.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, _i64,
+                                        _i64, ctypes.POINTER(ctypes.c_uint8)]
+    lib.oracle_layernorm_forward.argtypes = [_i64, _i64, _dp, _dp, _dp, ctypes.c_double, _dp,
+                                             _dp, _dp]
+    lib.oracle_layernorm_backward.argtypes = [_i64, _i64, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp]
     return lib
 
 
@@ -296,3 +304,85 @@ def row_linear(X_shards, W_shards, b, dZ=None):
                                        _ptr(db))
         out.update(dX=dX, dW=dW, db=db)
     return out
+
+
+# ---- sequence-parallel LayerNorm / Dropout sublayer ---------------------------
+# Out = X + Dropout(MLP(LN(X))), LayerNorm and Dropout per token chunk
+# ("Megatron-LM：NVIDIA 的大规模并行训练方案", 并行训练范式 / 序列并行); the
+# composition is the usual pre-LayerNorm residual block (a reading).
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 (Salmon et al., SC'11): 4 output words for a 4-word counter
+    and a 2-word key."""
+    lib = _load()
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in counter])
+    k = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib.oracle_philox4x32_10(c, k, o)
+    return [int(x) for x in o]
+
+
+def dropout_threshold(p: float) -> int:
+    """keep iff the Philox word is below floor((1 - p) * 2^32)."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return int(np.floor((1.0 - float(p)) * 4294967296.0))
+
+
+def dropout_keep(T: int, h: int, p: float, seed: int, offset: int = 0, e0: int = 0,
+                 count: int | None = None) -> np.ndarray:
+    """0/1 keep mask of elements [e0, e0 + count) of a [T, h] tensor (all by default)."""
+    lib = _load()
+    n = T * h - e0 if count is None else count
+    out = np.empty(max(n, 0), dtype=np.uint8)
+    if n > 0:
+        lib.oracle_dropout_keep(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                dropout_threshold(p), int(e0), int(n),
+                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return out
+
+
+def layernorm(X, gamma, beta, eps: float, dXn=None):
+    """LayerNorm over the last dimension: Xn, mean, rstd; with dXn the backward
+    dX, dgamma, dbeta too."""
+    lib = _load()
+    X = _f64(X); gamma = _f64(gamma); beta = _f64(beta)
+    T, h = X.shape
+    if gamma.shape != (h,) or beta.shape != (h,):
+        raise ValueError("gamma and beta must be [h]")
+    Xn = np.empty((T, h)); mean = np.empty(T); rstd = np.empty(T)
+    lib.oracle_layernorm_forward(T, h, _ptr(X), _ptr(gamma), _ptr(beta), float(eps), _ptr(Xn),
+                                 _ptr(mean), _ptr(rstd))
+    out = {"Xn": Xn, "mean": mean, "rstd": rstd}
+    if dXn is not None:
+        dXn = _f64(dXn)
+        dX = np.empty((T, h)); dg = np.empty(h); db = np.empty(h)
+        lib.oracle_layernorm_backward(T, h, _ptr(X), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                                      _ptr(dXn), _ptr(dX), _ptr(dg), _ptr(db))
+        out.update(dX=dX, dgamma=dg, dbeta=db)
+    return out
+
+
+def sp_layer(X, gamma, beta, eps, A_shards, b1, B_shards, b2, p, seed, offset=0, dOut=None):
+    """Out = X + Dropout(MLP(LN(X))); with dOut the backward of every input:
+    dX (through both paths), dgamma, dbeta, dA_i, db1, dB_i, db2.  Also returns
+    the intermediates Xn, Z, keep."""
+    X = _f64(X)
+    T, h = X.shape
+    ln = layernorm(X, gamma, beta, eps)
+    keep = dropout_keep(T, h, p, seed, offset).reshape(T, h).astype(np.float64)
+    scale = 1.0 / (1.0 - float(p))
+    if dOut is None:
+        blk = forward(ln["Xn"], A_shards, b1, B_shards, b2)
+        Out = X + keep * scale * blk["Z"]
+        return {"Out": Out, "Xn": ln["Xn"], "Z": blk["Z"], "keep": keep, "mean": ln["mean"],
+                "rstd": ln["rstd"]}
+    dOut = _f64(dOut)
+    dZ = dOut * keep * scale                      # dropout backward
+    blk = forward_backward(ln["Xn"], A_shards, b1, B_shards, b2, dZ)
+    lnb = layernorm(X, gamma, beta, eps, dXn=blk["dX"])
+    Out = X + keep * scale * blk["Z"]
+    return {"Out": Out, "Xn": ln["Xn"], "Z": blk["Z"], "keep": keep, "dZ": dZ,
+            "dXn": blk["dX"], "dX": lnb["dX"] + dOut, "dgamma": lnb["dgamma"],
+            "dbeta": lnb["dbeta"], "dA": blk["dA"], "db1": blk["db1"], "dB": blk["dB"],
+            "db2": blk["db2"], "mean": ln["mean"], "rstd": ln["rstd"]}

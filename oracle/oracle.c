@@ -40,6 +40,11 @@
  *     ([CH2] 2.2: the QKV projection column parallel, the output projection
  *     row parallel); their biases follow the same placement as b1 and b2.
  *     Pinned by tests/test_oracle_linear_pins.py.
+ *   - Sequence parallelism places LayerNorm and Dropout on each rank's token
+ *     chunk ([FGO-SP]); the sublayer around the block is read as the usual
+ *     pre-LayerNorm residual block Out = X + Dropout(MLP(LN(X))), LayerNorm
+ *     with the biased variance and eps, Dropout with a Philox4x32-10 mask
+ *     (details at oracle_dropout_keep).  Pinned by tests/test_oracle_sp_pins.py.
  *
  * Parallelism: OpenMP over output rows only; every output element is a
  * plain sum taken in index order.
@@ -454,5 +459,120 @@ void oracle_row_linear_backward(int64_t T, int64_t in, int64_t out, int t,
         double s = 0.0;
         for (int64_t r = 0; r < T; ++r) s += dZ[r * out + n];
         db[n] = s;
+    }
+}
+
+/* ---- sequence-parallel LayerNorm / Dropout sublayer --------------------------
+ * "在张量并行的基础上，LayerNorm 和 Dropout 沿序列维度分布" ([FGO-SP] 序列并行):
+ * with sequence parallelism the LayerNorm before the column-parallel GEMM and
+ * the Dropout after the row-parallel GEMM run on each rank's token chunk.  The
+ * pages give no formula for the sublayer; the reading taken (the usual
+ * pre-LayerNorm residual block) is
+ *
+ *   Xn  = LN(X) = (X - mean) * rstd * gamma + beta,   per token row, over h
+ *         mean = sum_n X[n] / h,  var = sum_n (X[n] - mean)^2 / h,
+ *         rstd = 1 / sqrt(var + eps)
+ *   Z   = MLP(Xn)                      (the block above, b2 included)
+ *   Out = X + Dropout(Z),  Dropout(z) = keep ? z / (1 - p) : 0
+ *
+ * keep for element (r, n) of the [T, h] output: Philox4x32-10 (Salmon, Moraes,
+ * Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11) with
+ * key (seed_lo, seed_hi) and counter (lo, hi, 0, 0) of c = offset + e / 4,
+ * e = r * h + n; word e % 4 of the output u, and keep iff u < thresh, thresh =
+ * floor((1 - p) * 2^32) (an integer in [0, 2^32]).
+ */
+
+static void philox_round(uint32_t *c, const uint32_t *k) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    const uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    const uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+}
+
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k[0] += 0x9E3779B9u;
+            k[1] += 0xBB67AE85u;
+        }
+        philox_round(c, k);
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/* keep[e] (0/1) for e in [0, count) of a [T, h] tensor starting at element e0 */
+void oracle_dropout_keep(uint64_t seed, uint64_t offset, uint64_t thresh, int64_t e0,
+                         int64_t count, uint8_t *keep) {
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    for (int64_t i = 0; i < count; ++i) {
+        const uint64_t e = (uint64_t)(e0 + i);
+        const uint64_t c = offset + e / 4;
+        const uint32_t ctr[4] = {(uint32_t)c, (uint32_t)(c >> 32), 0u, 0u};
+        uint32_t u[4];
+        oracle_philox4x32_10(ctr, key, u);
+        keep[i] = (uint64_t)u[e % 4] < thresh ? 1 : 0;
+    }
+}
+
+/* LayerNorm forward over rows of X [T, h]: Xn, and the per-row mean and rstd */
+void oracle_layernorm_forward(int64_t T, int64_t h, const double *X, const double *gamma,
+                              const double *beta, double eps, double *Xn, double *mean,
+                              double *rstd) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        const double *x = X + r * h;
+        double s = 0.0;
+        for (int64_t n = 0; n < h; ++n) s += x[n];
+        const double mu = s / (double)h;
+        double v = 0.0;
+        for (int64_t n = 0; n < h; ++n) v += (x[n] - mu) * (x[n] - mu);
+        const double rs = 1.0 / sqrt(v / (double)h + eps);
+        for (int64_t n = 0; n < h; ++n) Xn[r * h + n] = (x[n] - mu) * rs * gamma[n] + beta[n];
+        mean[r] = mu;
+        rstd[r] = rs;
+    }
+}
+
+/* LayerNorm backward: dX from dXn, and dgamma, dbeta (column sums over rows)
+ *   xhat = (x - mean) * rstd,  g = dXn * gamma,
+ *   dX = rstd * (g - mean_n(g) - xhat * mean_n(g * xhat))
+ *   dgamma = sum_r dXn * xhat,  dbeta = sum_r dXn */
+void oracle_layernorm_backward(int64_t T, int64_t h, const double *X, const double *gamma,
+                               const double *mean, const double *rstd, const double *dXn,
+                               double *dX, double *dgamma, double *dbeta) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T; ++r) {
+        const double *x = X + r * h;
+        const double *dy = dXn + r * h;
+        double sg = 0.0, sgx = 0.0;
+        for (int64_t n = 0; n < h; ++n) {
+            const double xh = (x[n] - mean[r]) * rstd[r];
+            const double g = dy[n] * gamma[n];
+            sg += g;
+            sgx += g * xh;
+        }
+        const double mg = sg / (double)h, mgx = sgx / (double)h;
+        for (int64_t n = 0; n < h; ++n) {
+            const double xh = (x[n] - mean[r]) * rstd[r];
+            dX[r * h + n] = rstd[r] * (dy[n] * gamma[n] - mg - xh * mgx);
+        }
+    }
+    for (int64_t n = 0; n < h; ++n) {
+        double sgm = 0.0, sbt = 0.0;
+        for (int64_t r = 0; r < T; ++r) {
+            const double xh = (X[r * h + n] - mean[r]) * rstd[r];
+            sgm += dXn[r * h + n] * xh;
+            sbt += dXn[r * h + n];
+        }
+        dgamma[n] = sgm;
+        dbeta[n] = sbt;
     }
 }

@@ -9,6 +9,7 @@ import pytest
 import oracle
 import test_oracle_linear_pins as lin
 import test_oracle_pins as pins
+import test_oracle_sp_pins as sp
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -43,6 +44,20 @@ MUTATIONS = [
      "for (int64_t r = 1; r < T; ++r) {\n                const double x = Xi[r * ii + k];"),
     ("row linear: db from the first row only", "for (int64_t r = 0; r < T; ++r) s += dZ[r * out + n];",
      "for (int64_t r = 0; r < 1; ++r) s += dZ[r * out + n];"),
+    # sequence-parallel LayerNorm / Dropout sublayer
+    ("philox: Weyl key constant", "k[0] += 0x9E3779B9u;", "k[0] += 0x9E3779B8u;"),
+    ("philox: second multiplier on the wrong word", "(uint64_t)0xCD9E8D57u * c[2];",
+     "(uint64_t)0xCD9E8D57u * c[0];"),
+    ("dropout: next output word", "keep[i] = (uint64_t)u[e % 4] < thresh", "keep[i] = (uint64_t)u[(e + 1) % 4] < thresh"),
+    ("dropout: counter off by one element", "const uint64_t c = offset + e / 4;",
+     "const uint64_t c = offset + (e + 1) / 4;"),
+    ("layernorm: unbiased variance", "const double rs = 1.0 / sqrt(v / (double)h + eps);",
+     "const double rs = 1.0 / sqrt(v / (double)(h - 1) + eps);"),
+    ("layernorm: beta dropped", "Xn[r * h + n] = (x[n] - mu) * rs * gamma[n] + beta[n];",
+     "Xn[r * h + n] = (x[n] - mu) * rs * gamma[n];"),
+    ("layernorm backward: mean term dropped", "dX[r * h + n] = rstd[r] * (dy[n] * gamma[n] - mg - xh * mgx);",
+     "dX[r * h + n] = rstd[r] * (dy[n] * gamma[n] - xh * mgx);"),
+    ("layernorm backward: dgamma without xhat", "sgm += dXn[r * h + n] * xh;", "sgm += dXn[r * h + n];"),
 ]
 
 PIN_CALLS = [
@@ -53,6 +68,12 @@ PIN_CALLS = [
     lambda: pins.test_b2_added_once(),
     lambda: lin.test_column_linear_exact_integers(3, 4, 6, 2),
     lambda: lin.test_row_linear_exact_integers(3, 6, 4, 2),
+    lambda: sp.test_philox_known_answers(*sp.KAT[2]),
+    lambda: sp.test_dropout_counter_layout(),
+    lambda: sp.test_layernorm_two_features_exact(),
+    lambda: sp.test_layernorm_moments_and_affine_invariance(),
+    lambda: sp.test_layernorm_backward_finite_differences(),
+    lambda: sp.test_sp_layer_backward_finite_differences(),
 ]
 
 
