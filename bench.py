@@ -16,6 +16,11 @@ attention projections, e.g. qkv_175b: the 175B-class QKV projection 12288 x
 projection, row parallel).  One step is then that layer's forward and
 backward (3 GEMMs of 2*T*in*out FLOP and the bias gradient).
 
+--sp-layer wraps the MLP workload in the sequence-parallel sublayer
+Out = X + Dropout(MLP(LN(X))) (LayerNorm and dropout per token chunk); the
+FLOP count stays the block's 12*T*h*f (the LayerNorm and dropout passes are
+timed but counted as no FLOP).
+
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded token sample of the same layer per step (same metric and unit).
 Under torchrun with N > 1 every rank runs an independent replica of the
@@ -36,6 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s and tokens/s on 1 GB300; % of BF16 dense peak"
+SP_EPS, SP_P, SP_SEED = 1e-5, 0.1, 1234
 LINEAR_METRIC = ("TP linear layer (attention projection) fwd+bwd TFLOP/s and tokens/s on 1 GB300; "
                  "% of BF16 dense peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -53,6 +59,9 @@ def parse_args():
     ap.add_argument("--ffn", type=int, help="override f")
     ap.add_argument("--t", type=int, help="override the shard count")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sp-layer", action="store_true",
+                    help="run the sequence-parallel sublayer Out = X + Dropout(MLP(LN(X))) around "
+                         "the MLP workload (dropout p = 0.1, eps = 1e-5)")
     ap.add_argument("--recompute", action="store_true",
                     help="selective recompute: keep only Y between passes, rebuild H in backward")
     ap.add_argument("--split-min-kblocks", type=int, default=None,
@@ -319,12 +328,32 @@ class LinearOracleSample(OracleSample):
         return f"{w.split} split, in={w.in_features}, out={w.out_features}, t={w.t}"
 
 
-def oracle_sample(w, inputs):
-    return LinearOracleSample(w, inputs) if hasattr(w, "split") else OracleSample(w, inputs)
+class SpOracleSample(OracleSample):
+    """The fp64 oracle of the sequence-parallel sublayer on the first T_s tokens."""
+
+    def __init__(self, w, inputs):
+        super().__init__(w, inputs)
+        self.gamma = inputs["gamma"].double().numpy()
+        self.beta = inputs["beta"].double().numpy()
+
+    def run(self, tokens: int) -> float:
+        t0 = time.perf_counter()
+        self.oracle.sp_layer(self.X[:tokens], self.gamma, self.beta, SP_EPS, self.A, self.b1,
+                             self.B, self.b2, SP_P, SP_SEED, dOut=self.dZ[:tokens])
+        return time.perf_counter() - t0
+
+    def describe(self) -> str:
+        return f"LN + MLP + dropout + residual, h={self.w.hidden}, f={self.w.ffn}, t={self.w.t}"
 
 
-def cpu_baseline(w, inputs, target_s: float) -> dict:
-    smp = oracle_sample(w, inputs)
+def oracle_sample(w, inputs, sp_layer=False):
+    if hasattr(w, "split"):
+        return LinearOracleSample(w, inputs)
+    return SpOracleSample(w, inputs) if sp_layer else OracleSample(w, inputs)
+
+
+def cpu_baseline(w, inputs, target_s: float, sp_layer=False) -> dict:
+    smp = oracle_sample(w, inputs, sp_layer)
     tok = smp.calibrate(target_s)
     dt = smp.run(tok)
     flops = smp.flops(tok)
@@ -383,10 +412,13 @@ def run_reference(args, torch):
         inputs = make_linear_inputs(w, 0)
         metric, config = LINEAR_METRIC, linear_config(w, "host memory (CPU oracle)")
     else:
+        from tensor_transformer_mlp_gemm_gb300.inputs import make_sp_inputs
         w = pick_workload(args)
-        inputs = make_inputs(w, 0)
+        inputs = make_sp_inputs(w, 0) if args.sp_layer else make_inputs(w, 0)
         metric, config = METRIC, workload_config(w, "host memory (CPU oracle)")
-    smp = oracle_sample(w, inputs)
+        if args.sp_layer:
+            config = {**config, **sp_config()}
+    smp = oracle_sample(w, inputs, args.sp_layer)
     per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
     tok = smp.calibrate(per_step, start=min(w.tokens, max(4, smp.cores // 2)))
     for _ in range(args.warmup):
@@ -468,6 +500,55 @@ class MlpRunner:
                              blk.db1, blk.dB, blk.db2, stream)
 
 
+def sp_config():
+    return {"sublayer": "Out = X + Dropout(MLP(LN(X))), LayerNorm and dropout per token chunk",
+            "layernorm_eps": SP_EPS, "dropout_p": SP_P, "dropout_seed": SP_SEED,
+            "flop_count": "the block's 12*T*h*f; LayerNorm and dropout passes timed, no FLOP"}
+
+
+class SpRunner(MlpRunner):
+    """One step = tpmlp_sp_forward + tpmlp_sp_backward of the sublayer."""
+
+    def __init__(self, args, dev):
+        from tensor_transformer_mlp_gemm_gb300 import binding
+        from tensor_transformer_mlp_gemm_gb300.inputs import make_sp_inputs
+        from tensor_transformer_mlp_gemm_gb300.sp import DeviceSPLayer
+        self.binding = binding
+        self.w = w = pick_workload(args)
+        self.inputs = make_sp_inputs(w, 0)
+        self.recompute = False
+        self.lay = DeviceSPLayer(w, self.inputs, device=dev, eps=SP_EPS, dropout_p=SP_P,
+                                 seed=SP_SEED)
+        T, h, f = w.tokens, w.hidden, w.ffn
+        self.tokens = T
+        self.metric = METRIC
+        self.flops_step = 12.0 * T * h * f
+        self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
+        self.gemm_flops = 2.0 * T * h * f
+        self.colsum_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
+        # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes dX
+        self.ln_bytes = 2 * T * h * 2 + 4 * T * h * 2
+        self.dropout_bytes = 2 * T * h * 2
+        self.l2_note = (f"inputs larger than L2 (bf16 weights {2 * h * f * 2 / 1e9:.2f} GB, "
+                        f"activations {(3 * T * f + 4 * T * h) * 2 / 1e9:.2f} GB per step)")
+        self.ins, self.outs = ("X", "dOut"), ("Out", "dX")
+
+    def config(self):
+        return {**workload_config(self.w, self.l2_note), **sp_config()}
+
+    def buffers(self, name):
+        return getattr(self.lay, name)
+
+    def step(self, stream):
+        self.lay.step(stream)
+
+    def forward(self, B, stream):
+        self.lay.forward(stream, X=B["X"], Out=B["Out"])
+
+    def backward(self, B, stream):
+        self.lay.backward(stream, dOut=B["dOut"], X=B["X"], dX=B["dX"])
+
+
 class LinearRunner:
     """One step = forward + backward of one tensor-parallel linear layer."""
 
@@ -518,7 +599,12 @@ def run_ours(args, torch):
     torch.cuda.set_device(dev)
     if args.split_min_kblocks is not None:
         binding.tpmlp_set_split_min_kblocks(args.split_min_kblocks)
-    run = LinearRunner(args, dev) if is_linear(args) else MlpRunner(args, dev)
+    if is_linear(args):
+        run = LinearRunner(args, dev)
+    elif args.sp_layer:
+        run = SpRunner(args, dev)
+    else:
+        run = MlpRunner(args, dev)
     w = run.w
     stream = torch.cuda.current_stream(dev)
     T = run.tokens
@@ -579,6 +665,11 @@ def run_ours(args, torch):
         cs_ms = kms["bias_grad"] / args.steps
         kernels["bias_grad"]["gb_per_s"] = run.colsum_bytes / (cs_ms / 1e3) / 1e9
         kernels["bias_grad"]["frac_of_hbm"] = kernels["bias_grad"]["gb_per_s"] / peaks["hbm_gbs"]
+    for name, attr in (("layernorm", "ln_bytes"), ("dropout_bwd", "dropout_bytes")):
+        if name in kernels and hasattr(run, attr):
+            per_step = kms[name] / args.steps
+            kernels[name]["gb_per_s"] = getattr(run, attr) / (per_step / 1e3) / 1e9
+            kernels[name]["frac_of_hbm"] = kernels[name]["gb_per_s"] / peaks["hbm_gbs"]
     for name in run.gemm_kinds:
         if name in kernels:
             kernels[name]["tflops"] = run.gemm_flops / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
@@ -660,7 +751,7 @@ def run_ours(args, torch):
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            cpu = cpu_baseline(w, run.inputs, args.cpu_seconds)
+            cpu = cpu_baseline(w, run.inputs, args.cpu_seconds, args.sp_layer)
         line = {"metric": run.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

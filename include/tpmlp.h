@@ -248,6 +248,61 @@ tpmlp_status tpmlp_row_linear_backward(const tpmlp_linear_dims* dims,
                                        void* const* dW_shards, void* db,
                                        void* workspace, void* stream);
 
+/* ---- Sequence-parallel LayerNorm / Dropout sublayer ---------------------------
+ * "Megatron-LM：NVIDIA 的大规模并行训练方案", "并行训练范式 / 序列并行": on top
+ * of tensor parallelism, LayerNorm and Dropout are distributed along the
+ * sequence dimension, each rank working on its token chunk.  The sublayer
+ * around the block is the pre-LayerNorm residual block
+ *
+ *   Out = X + Dropout(MLP(LN(X)))
+ *   LN(X) = (X - mean) * rstd * gamma + beta per token row over h,
+ *           mean and var the row's mean and (biased) variance, rstd = 1/sqrt(var + eps)
+ *   Dropout(z) = keep ? z / (1 - p) : 0
+ *
+ * keep for element (r, n) of the [T, h] output, e = r * h + n (r the token
+ * row over all chunks): Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11) with key
+ * (seed_lo, seed_hi) and counter (lo, hi, 0, 0) of offset + e / 4; word e % 4
+ * of its output is compared with floor((1 - p) * 2^32) (keep iff below).
+ * The same element keeps the same mask in the forward and the backward call.
+ *
+ * The forward pass runs LN per token chunk, then the block on LN(X) with the
+ * dropout and the residual add fused into the row GEMM's epilogue; the
+ * backward pass undoes the dropout on dOut, runs the block's backward pass,
+ * then LN's backward with the residual gradient dOut added:
+ *   dX = LN'(dXn) + dOut,  dgamma = sum_r dXn * xhat,  dbeta = sum_r dXn
+ * Layouts, chunking, conventions and errors as tpmlp_forward / tpmlp_backward,
+ * with h <= 16384 (else TPMLP_ERR_UNSUPPORTED), eps >= 0 and 0 <= p < 1
+ * (else TPMLP_ERR_INVALID_ARG).  gamma, beta [h] bf16; dgamma, dbeta [h] fp32.
+ * The workspace (tpmlp_sp_workspace_bytes) holds the block's workspace plus
+ * LN(X), the row statistics, dZ and the gradient of LN(X); it must be kept
+ * from the forward call to the matching backward call. */
+typedef struct {
+    float eps;           /* LayerNorm epsilon (e.g. 1e-5) */
+    double dropout_p;    /* probability of dropping an element, 0 <= p < 1 */
+    uint64_t seed;       /* Philox key */
+    uint64_t offset;     /* Philox counter offset, in blocks of 4 elements */
+} tpmlp_sp_params;
+
+size_t tpmlp_sp_workspace_bytes(const tpmlp_dims* dims);
+/* Byte offsets in that workspace of LN(X) and of dZ (= dOut with the dropout
+ * undone, written by tpmlp_sp_backward), each a [T, h] bf16 tensor stored
+ * chunk after chunk.  Either output may be NULL. */
+tpmlp_status tpmlp_sp_workspace_layout(const tpmlp_dims* dims, size_t* xn_offset,
+                                       size_t* dz_offset);
+tpmlp_status tpmlp_sp_forward(const tpmlp_dims* dims, const tpmlp_sp_params* sp,
+                              const void* const* X, const void* gamma, const void* beta,
+                              const void* const* A_shards, const void* b1,
+                              const void* const* B_shards, const void* b2, int t,
+                              void* const* Out, void* workspace, void* stream);
+tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_params* sp,
+                               const void* const* dOut, const void* const* X,
+                               const void* gamma, const void* const* A_shards,
+                               const void* const* B_shards, void* workspace,
+                               void* const* dX, void* dgamma, void* dbeta,
+                               void* const* dA_shards, void* db1,
+                               void* const* dB_shards, void* db2, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* tpmlp_status_string(tpmlp_status s);
 
@@ -325,7 +380,9 @@ enum {
     TPMLP_KERNEL_LINEAR_FWD = 7,  /* linear layers: Y_i = X.W_i + b, Z = sum_i X_i.W_i + b */
     TPMLP_KERNEL_LINEAR_DGRAD = 8,  /* linear layers: dX = sum_i dY_i.W_i^T, dX_i = dZ.W_i^T */
     TPMLP_KERNEL_LINEAR_WGRAD = 9,  /* linear layers: dW_i */
-    TPMLP_KERNEL_KINDS = 10
+    TPMLP_KERNEL_LAYERNORM = 10,    /* sequence-parallel sublayer: LN forward, LN backward */
+    TPMLP_KERNEL_DROPOUT_BWD = 11,  /* sequence-parallel sublayer: dZ from dOut and the mask */
+    TPMLP_KERNEL_KINDS = 12
 };
 tpmlp_status tpmlp_profile_begin(int capacity);
 int tpmlp_profile_end(double* ms, int* launches, int nkinds);

@@ -27,7 +27,7 @@ TPMLP_ERR_UNSUPPORTED = 2
 TPMLP_ERR_CUDA = 3
 TPMLP_ERR_TIMEOUT = 4
 
-KERNEL_KINDS = 10
+KERNEL_KINDS = 12
 
 # every symbol include/tpmlp.h declares
 EXPORTED = (
@@ -38,6 +38,7 @@ EXPORTED = (
     "tpmlp_recompute_workspace_bytes", "tpmlp_forward_recompute", "tpmlp_backward_recompute",
     "tpmlp_linear_workspace_bytes", "tpmlp_column_linear_forward", "tpmlp_column_linear_backward",
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
+    "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
 )
 
 
@@ -52,6 +53,11 @@ class tpmlp_linear_dims(ctypes.Structure):
                 ("seq_chunks", ctypes.c_int32)]
 
 
+class tpmlp_sp_params(ctypes.Structure):
+    _fields_ = [("eps", ctypes.c_float), ("dropout_p", ctypes.c_double),
+                ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
 class TpmlpError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -63,6 +69,7 @@ _vpp = ctypes.POINTER(ctypes.c_void_p)
 _dims_p = ctypes.POINTER(tpmlp_dims)
 _sz_p = ctypes.POINTER(ctypes.c_size_t)
 _ldims_p = ctypes.POINTER(tpmlp_linear_dims)
+_sp_p = ctypes.POINTER(tpmlp_sp_params)
 
 _lib.tpmlp_workspace_bytes.restype = ctypes.c_size_t
 _lib.tpmlp_workspace_bytes.argtypes = [_dims_p]
@@ -99,6 +106,16 @@ _lib.tpmlp_kernel_name.restype = ctypes.c_char_p
 _lib.tpmlp_kernel_name.argtypes = [ctypes.c_int]
 _lib.tpmlp_column_sums_noalloc.restype = ctypes.c_int
 _lib.tpmlp_column_sums_noalloc.argtypes = [_vp, ctypes.c_int64, ctypes.c_int64, _vp, _vp]
+_lib.tpmlp_sp_workspace_bytes.restype = ctypes.c_size_t
+_lib.tpmlp_sp_workspace_bytes.argtypes = [_dims_p]
+_lib.tpmlp_sp_workspace_layout.restype = ctypes.c_int
+_lib.tpmlp_sp_workspace_layout.argtypes = [_dims_p, _sz_p, _sz_p]
+_lib.tpmlp_sp_forward.restype = ctypes.c_int
+_lib.tpmlp_sp_forward.argtypes = [_dims_p, _sp_p, _vpp, _vp, _vp, _vpp, _vp, _vpp, _vp, ctypes.c_int,
+                                  _vpp, _vp, _vp]
+_lib.tpmlp_sp_backward.restype = ctypes.c_int
+_lib.tpmlp_sp_backward.argtypes = [_dims_p, _sp_p, _vpp, _vpp, _vp, _vpp, _vpp, _vp, _vpp, _vp, _vp,
+                                   _vpp, _vp, _vpp, _vp, _vp]
 _lib.tpmlp_linear_workspace_bytes.restype = ctypes.c_size_t
 _lib.tpmlp_linear_workspace_bytes.argtypes = [_ldims_p]
 for _name in ("tpmlp_column_linear_forward", "tpmlp_row_linear_forward"):
@@ -284,3 +301,38 @@ def tpmlp_row_linear_backward(dims, dZ, X_shards, W_shards, dX_shards, dW_shards
                                           _arr(W_shards), _arr(dX_shards), _arr(dW_shards),
                                           _ptr(db), _ptr(workspace), _stream(stream)),
            "tpmlp_row_linear_backward")
+
+
+def make_sp_params(eps: float = 1e-5, dropout_p: float = 0.1, seed: int = 0,
+                   offset: int = 0) -> tpmlp_sp_params:
+    return tpmlp_sp_params(float(eps), float(dropout_p), int(seed) & (2**64 - 1),
+                           int(offset) & (2**64 - 1))
+
+
+def tpmlp_sp_workspace_bytes(dims: tpmlp_dims) -> int:
+    return int(_lib.tpmlp_sp_workspace_bytes(ctypes.byref(dims)))
+
+
+def tpmlp_sp_workspace_layout(dims: tpmlp_dims) -> tuple[int, int]:
+    xn, dz = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.tpmlp_sp_workspace_layout(ctypes.byref(dims), ctypes.byref(xn), ctypes.byref(dz)),
+           "tpmlp_sp_workspace_layout")
+    return xn.value, dz.value
+
+
+def tpmlp_sp_forward(dims, sp, X, gamma, beta, A_shards, b1, B_shards, b2, t, Out, workspace,
+                     stream=None) -> None:
+    """X, Out: lists of seq_chunks tensors; A_shards, B_shards: lists of t tensors."""
+    _check(_lib.tpmlp_sp_forward(ctypes.byref(dims), ctypes.byref(sp), _arr(X), _ptr(gamma),
+                                 _ptr(beta), _arr(A_shards), _ptr(b1), _arr(B_shards), _ptr(b2),
+                                 int(t), _arr(Out), _ptr(workspace), _stream(stream)),
+           "tpmlp_sp_forward")
+
+
+def tpmlp_sp_backward(dims, sp, dOut, X, gamma, A_shards, B_shards, workspace, dX, dgamma, dbeta,
+                      dA_shards, db1, dB_shards, db2, stream=None) -> None:
+    _check(_lib.tpmlp_sp_backward(ctypes.byref(dims), ctypes.byref(sp), _arr(dOut), _arr(X),
+                                  _ptr(gamma), _arr(A_shards), _arr(B_shards), _ptr(workspace),
+                                  _arr(dX), _ptr(dgamma), _ptr(dbeta), _arr(dA_shards), _ptr(db1),
+                                  _arr(dB_shards), _ptr(db2), _stream(stream)),
+           "tpmlp_sp_backward")

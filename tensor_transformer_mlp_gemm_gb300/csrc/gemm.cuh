@@ -300,7 +300,7 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int r, const float 
 template <int EPI>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int part, long long row,
                                               int m, int n, float (&x)[32], float (&x2)[32]) {
-    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS) {
+    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS || EPI == EPI_BIAS_DROP_RES) {
         const __nv_bfloat16* b =
             static_cast<const __nv_bfloat16*>(p.bias) + n + g * p.bias_group_stride;
 #pragma unroll
@@ -315,6 +315,35 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
         if constexpr (EPI == EPI_BIAS_GELU) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) x2[j] = gelu_f(x[j]);
+        }
+    }
+    if constexpr (EPI == EPI_BIAS_DROP_RES) {
+        // Out = in0 + Dropout(acc + bias): the 32 columns of this row are the
+        // elements e0 .. e0 + 31 of the [M, N] output, e0 = m * N + n (a multiple
+        // of 4), i.e. eight Philox counters offset + e0 / 4 + q
+        if (m < p.M) {
+            const uint64_t e0 = static_cast<uint64_t>(m) * static_cast<uint64_t>(p.N) +
+                                static_cast<uint64_t>(n);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const PhiloxOut o = philox4x32_10(p.drop.offset + e0 / 4 + q, p.drop.seed);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool keep = static_cast<uint64_t>(o.w[j]) < p.drop.thresh;
+                    x[4 * q + j] = keep ? x[4 * q + j] * p.drop.scale : 0.0f;
+                }
+            }
+            const __nv_bfloat16* res =
+                static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (n + 8 * q < p.N) {
+                    float rf[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4*>(res + 8 * q), rf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] += rf[j];
+                }
+            }
         }
     }
     if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {

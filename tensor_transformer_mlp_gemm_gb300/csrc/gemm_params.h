@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "philox.cuh"
+
 namespace tpmlp {
 
 // A CTA pair (cluster of 2) computes a CLUSTER_M x BN tile with
@@ -56,7 +58,8 @@ enum Epi : int {
     EPI_DGELU = 3,      // out 1 = bf16(acc * GeLU'(in0))
     EPI_BF16 = 4,       // out 1 = bf16(acc)
     EPI_F32 = 5,        // out 1 = acc (fp32)
-    EPI_DGELU_H = 6     // out 1 = bf16(acc * GeLU'(in0)), out 2 = bf16(GeLU(in0)) (recompute)
+    EPI_DGELU_H = 6,    // out 1 = bf16(acc * GeLU'(in0)), out 2 = bf16(GeLU(in0)) (recompute)
+    EPI_BIAS_DROP_RES = 7  // out 1 = bf16(in0 + dropout(acc + bias)) (sequence-parallel sublayer)
 };
 
 // Error-word bits (which role gave up).
@@ -91,6 +94,7 @@ struct GemmParams {
     int out_part;            // PART_GROUP or PART_ROW
     int out_rows_per_part;   // rows per output chunk for PART_ROW
     int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU, EPI_BIAS)
+    DropoutParams drop;      // EPI_BIAS_DROP_RES: mask of element (m, n) = Philox word of m * N + n
     // control
     unsigned int* err;
     unsigned long long timeout_ns;
@@ -108,6 +112,8 @@ struct GemmParams {
 cudaError_t launch_column_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_row_fwd(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_dgrad_h(const GemmParams& p, cudaStream_t stream);
+//   row_fwd_dropout: A K-major, B MN-major, EPI_BIAS_DROP_RES (Out = X + Dropout(Z))
+cudaError_t launch_row_fwd_dropout(const GemmParams& p, cudaStream_t stream);
 //   dgrad_h_recompute: A K-major, B K-major, EPI_DGELU_H (dY_i and H_i = GeLU(Y_i))
 cudaError_t launch_dgrad_h_recompute(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_dgrad_x(const GemmParams& p, cudaStream_t stream);

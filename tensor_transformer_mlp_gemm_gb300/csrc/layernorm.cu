@@ -1,0 +1,278 @@
+// layernorm.cu -- LayerNorm forward/backward and dropout backward of the
+// sequence-parallel sublayer (see layernorm.cuh).  One CTA of 256 threads per
+// token row in the forward pass; each thread holds up to eight 8-element
+// vectors of its row in registers, so X is read once and written once.
+// Reductions run warp-shuffle then one warp over the partial sums, always in
+// the same order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "layernorm.cuh"
+
+namespace tpmlp {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over the CTA's LN_THREADS threads; every thread gets the result.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    constexpr int W = LN_THREADS / 32;
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();  // the previous call's result has been read
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        float t = l < W ? red[l] : 0.0f;
+        t = warp_sum(t);
+        if (l == 0) red[W] = t;
+    }
+    __syncthreads();
+    return red[W];
+}
+
+// Token row r lives in chunk r / rows at local row r % rows.
+__device__ __forceinline__ long long chunk_row(long long r, long long rows, int& j) {
+    j = static_cast<int>(r / rows);
+    return r - static_cast<long long>(j) * rows;
+}
+
+__global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardParams p) {
+    __shared__ float red[LN_THREADS / 32 + 1];
+    const long long r = blockIdx.x;
+    int j;
+    const long long rr = chunk_row(r, p.x.rows, j);
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + rr * p.h;
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y[j]) + rr * p.h;
+    uint4 v[LN_MAX_VEC];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < p.h) {
+            v[i] = *reinterpret_cast<const uint4*>(x + c);
+            float f[8];
+            unpack8(v[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s += f[k];
+        }
+    }
+    const float mean = block_sum(s, red) / static_cast<float>(p.h);
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < p.h) {
+            float f[8];
+            unpack8(v[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q += (f[k] - mean) * (f[k] - mean);
+        }
+    }
+    const float var = block_sum(q, red) / static_cast<float>(p.h);
+    const float rs = 1.0f / sqrtf(var + p.eps);
+    const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
+    const __nv_bfloat16* bt = static_cast<const __nv_bfloat16*>(p.beta);
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < p.h) {
+            float f[8], g[8], b[8], o[8];
+            unpack8(v[i], f);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gm + c)), g);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(bt + c)), b);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = (f[k] - mean) * rs * g[k] + b[k];
+            *reinterpret_cast<uint4*>(y + c) = pack8(o);
+        }
+    }
+    if (threadIdx.x == 0) {
+        p.mean[r] = mean;
+        p.rstd[r] = rs;
+    }
+}
+
+// grid (T, ceil(h / 8 / LN_THREADS)): one 8-element vector per thread
+__global__ void __launch_bounds__(LN_THREADS) dropout_backward_kernel(const DropoutBackwardParams p) {
+    const long long r = blockIdx.x;
+    const int c = (blockIdx.y * LN_THREADS + threadIdx.x) * 8;
+    if (c >= p.h) return;
+    int j;
+    const long long rr = chunk_row(r, p.dout.rows, j);
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.dout.in[j]) + rr * p.h + c;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dz[j]) + rr * p.h + c;
+    const uint64_t e0 = static_cast<uint64_t>(r) * static_cast<uint64_t>(p.h) +
+                        static_cast<uint64_t>(c);  // a multiple of 8
+    float f[8];
+    unpack8(*reinterpret_cast<const uint4*>(src), f);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const PhiloxOut o = philox4x32_10(p.drop.offset + e0 / 4 + q, p.drop.seed);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool keep = static_cast<uint64_t>(o.w[k]) < p.drop.thresh;
+            f[4 * q + k] = keep ? f[4 * q + k] * p.drop.scale : 0.0f;
+        }
+    }
+    *reinterpret_cast<uint4*>(dst) = pack8(f);
+}
+
+// CTA b handles token rows [b * R, (b + 1) * R); dynamic shared memory holds
+// its partial dgamma (first h floats) and dbeta (next h floats), each column
+// owned by one thread.
+__global__ void __launch_bounds__(LN_THREADS) ln_backward_kernel(const LnBackwardParams p,
+                                                                 long long T) {
+    extern __shared__ float acc[];
+    __shared__ float red[LN_THREADS / 32 + 1];
+    const int h = p.h;
+    const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
+    uint4 gv[LN_MAX_VEC];
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < h) {
+            gv[i] = __ldg(reinterpret_cast<const uint4*>(gm + c));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                acc[c + k] = 0.0f;
+                acc[h + c + k] = 0.0f;
+            }
+        }
+    }
+    const long long r0 = static_cast<long long>(blockIdx.x) * p.rows_per_block;
+    const long long r1 = r0 + p.rows_per_block < T ? r0 + p.rows_per_block : T;
+    for (long long r = r0; r < r1; ++r) {
+        int j;
+        const long long rr = chunk_row(r, p.x.rows, j);
+        const long long off = rr * h;
+        const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + off;
+        const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(p.dxn[j]) + off;
+        const __nv_bfloat16* dres = static_cast<const __nv_bfloat16*>(p.dres[j]) + off;
+        __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(p.dx[j]) + off;
+        const float mean = p.mean[r], rs = p.rstd[r];
+        uint4 xv[LN_MAX_VEC], dv[LN_MAX_VEC];
+        float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < LN_MAX_VEC; ++i) {
+            const int c = (threadIdx.x + i * LN_THREADS) * 8;
+            if (c < h) {
+                xv[i] = *reinterpret_cast<const uint4*>(x + c);
+                dv[i] = *reinterpret_cast<const uint4*>(dy + c);
+                float xf[8], df[8], gf[8];
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
+                unpack8(gv[i], gf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float g = df[k] * gf[k];
+                    sg += g;
+                    sgx += g * (xf[k] - mean) * rs;
+                }
+            }
+        }
+        const float mg = block_sum(sg, red) / static_cast<float>(h);
+        const float mgx = block_sum(sgx, red) / static_cast<float>(h);
+#pragma unroll
+        for (int i = 0; i < LN_MAX_VEC; ++i) {
+            const int c = (threadIdx.x + i * LN_THREADS) * 8;
+            if (c < h) {
+                float xf[8], df[8], gf[8], rf[8], o[8];
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
+                unpack8(gv[i], gf);
+                unpack8(*reinterpret_cast<const uint4*>(dres + c), rf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float xh = (xf[k] - mean) * rs;
+                    o[k] = rs * (df[k] * gf[k] - mg - xh * mgx) + rf[k];
+                    acc[c + k] += df[k] * xh;
+                    acc[h + c + k] += df[k];
+                }
+                *reinterpret_cast<uint4*>(dx + c) = pack8(o);
+            }
+        }
+    }
+    float* part = p.part + static_cast<size_t>(blockIdx.x) * 2 * h;
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < h) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                part[c + k] = acc[c + k];
+                part[h + c + k] = acc[h + c + k];
+            }
+        }
+    }
+}
+
+// dgamma[c] = sum_b part[b][0][c], dbeta[c] = sum_b part[b][1][c], b in order
+__global__ void ln_finish_kernel(const float* part, int blocks, int h, float* dgamma,
+                                 float* dbeta) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= h) return;
+    float g = 0.0f, b = 0.0f;
+    for (int k = 0; k < blocks; ++k) {
+        g += part[static_cast<size_t>(k) * 2 * h + c];
+        b += part[static_cast<size_t>(k) * 2 * h + h + c];
+    }
+    dgamma[c] = g;
+    dbeta[c] = b;
+}
+
+}  // namespace
+
+cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    ln_forward_kernel<<<static_cast<unsigned>(T), LN_THREADS, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, int /*sm_count*/,
+                                    cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    const int vecs = (p.h + 7) / 8;
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((vecs + LN_THREADS - 1) / LN_THREADS));
+    dropout_backward_kernel<<<grid, LN_THREADS, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int blocks, float* dgamma,
+                               float* dbeta, cudaStream_t st) {
+    const size_t smem = 2 * static_cast<size_t>(p.h) * sizeof(float);
+    // per device; a host-side call, cheap enough to repeat
+    cudaError_t e = cudaFuncSetAttribute(ln_backward_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(2 * LN_MAX_H * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    ln_backward_kernel<<<blocks, LN_THREADS, smem, st>>>(p, T);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ln_finish_kernel<<<(p.h + 255) / 256, 256, 0, st>>>(p.part, blocks, p.h, dgamma, dbeta);
+    return cudaGetLastError();
+}
+
+}  // namespace tpmlp

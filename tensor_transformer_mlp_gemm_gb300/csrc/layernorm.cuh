@@ -1,0 +1,81 @@
+// layernorm.cuh -- the elementwise and row-reduction kernels of the
+// sequence-parallel sublayer Out = X + Dropout(MLP(LN(X))), each run per token
+// chunk ("Megatron-LM：NVIDIA 的大规模并行训练方案", 并行训练范式 / 序列并行).
+//   ln_forward:       Xn = (X - mean) * rstd * gamma + beta per token row, with
+//                     mean and rstd = 1 / sqrt(var + eps) (biased variance)
+//                     kept for the backward pass
+//   dropout_backward: dZ = keep ? dOut / (1 - p) : 0 (the forward's mask)
+//   ln_backward:      dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dOut,
+//                     g = dXn * gamma, plus per-CTA partial column sums of
+//                     dXn * xhat and dXn; ln_finish sums them in a fixed order
+//                     into dgamma and dbeta (no atomics anywhere).
+// All three are bound by HBM traffic.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "philox.cuh"
+
+namespace tpmlp {
+
+constexpr int LN_THREADS = 256;
+constexpr int LN_MAX_VEC = 8;                          // 8-element vectors per thread
+constexpr int LN_MAX_H = LN_THREADS * LN_MAX_VEC * 8;  // 16384
+constexpr int LN_MAX_CHUNKS = 8;
+
+struct LnChunks {
+    const void* in[LN_MAX_CHUNKS];
+    int n;
+    long long rows;  // rows per chunk
+};
+
+struct LnForwardParams {
+    LnChunks x;                  // bf16 [rows, h] per chunk
+    void* y[LN_MAX_CHUNKS];      // bf16 Xn, same chunking
+    const void* gamma;           // bf16 [h]
+    const void* beta;            // bf16 [h]
+    float* mean;                 // fp32 [T]
+    float* rstd;                 // fp32 [T]
+    int h;
+    float eps;
+};
+
+struct DropoutBackwardParams {
+    LnChunks dout;               // bf16 [rows, h] per chunk
+    void* dz[LN_MAX_CHUNKS];     // bf16, same chunking
+    int h;
+    DropoutParams drop;
+};
+
+struct LnBackwardParams {
+    LnChunks x;                  // bf16 X (the sublayer input)
+    const void* dxn[LN_MAX_CHUNKS];   // bf16 gradient of Xn, same chunking
+    const void* dres[LN_MAX_CHUNKS];  // bf16 gradient through the residual path (dOut)
+    void* dx[LN_MAX_CHUNKS];          // bf16 output
+    const void* gamma;           // bf16 [h]
+    const float* mean;
+    const float* rstd;
+    float* part;                 // fp32 [blocks][2][h] partial dgamma, dbeta
+    int h;
+    long long rows_per_block;
+};
+
+// Bytes of partial sums ln_backward needs for `blocks` CTAs.
+inline size_t ln_partial_bytes(int blocks, long long h) {
+    return static_cast<size_t>(blocks) * 2 * static_cast<size_t>(h) * sizeof(float);
+}
+// CTAs ln_backward uses for T rows on a GPU with sm_count SMs.
+inline int ln_backward_blocks(long long T, int sm_count) {
+    const long long b = 2LL * sm_count;
+    return static_cast<int>(T < b ? (T > 0 ? T : 1) : b);
+}
+
+cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st);
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, int sm_count,
+                                    cudaStream_t st);
+// Two launches: ln_backward over `blocks` CTAs, then the fixed-order finish.
+cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int blocks, float* dgamma,
+                               float* dbeta, cudaStream_t st);
+
+}  // namespace tpmlp

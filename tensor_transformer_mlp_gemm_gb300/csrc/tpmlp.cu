@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "abi_internal.h"
+#include "block_internal.h"
 #include "colsum.cuh"
 #include "gemm_params.h"
 #include "tpmlp.h"
@@ -220,15 +221,11 @@ bool attach_split(GemmParams& p, void* split_part, void* split_cnt) {
 
 }  // namespace abi
 
-namespace {
+namespace block {
 
 using namespace abi;
 
 // ---- workspace ---------------------------------------------------------------------------
-struct Layout {
-    size_t y, h, dy, part1, part2, split_part, split_cnt, total;
-};
-
 Layout layout_of(const tpmlp_dims& d) {
     Layout L;
     const size_t act = align256(static_cast<size_t>(d.tokens) * static_cast<size_t>(d.ffn) * 2);
@@ -258,19 +255,6 @@ tpmlp_status check_dims(const tpmlp_dims* d) {
     return TPMLP_OK;
 }
 
-// Device buffers one forward/backward pair works in.  The standard calls
-// carve them all out of one workspace; the recompute calls take the saved
-// pre-activation Y apart from a scratch area that holds the rest.
-struct Regions {
-    uint8_t* y;           // Y shards [t][T][fi] bf16 (kept from forward to backward)
-    uint8_t* h;           // H shards (kept in the standard calls; scratch with recompute)
-    uint8_t* dy;          // dY shards (scratch)
-    uint8_t* part1;       // db1 partial sums (scratch)
-    uint8_t* part2;       // db2 partial sums (scratch)
-    uint8_t* split_part;  // tail-split partial tiles (scratch)
-    uint8_t* split_cnt;   // tail-split counters (scratch)
-};
-
 Regions regions_of(uint8_t* ws, const Layout& L) {
     return Regions{ws + L.y, ws + L.h, ws + L.dy, ws + L.part1, ws + L.part2, ws + L.split_part,
                    ws + L.split_cnt};
@@ -292,10 +276,6 @@ bool attach_split(GemmParams& p, const Regions& R) {
     return abi::attach_split(p, R.split_part, R.split_cnt);
 }
 
-struct Shapes {
-    int T, h, f, t, fi, chunks, Tc;
-};
-
 Shapes shapes_of(const tpmlp_dims& d) {
     Shapes s;
     s.T = static_cast<int>(d.tokens);
@@ -308,9 +288,11 @@ Shapes shapes_of(const tpmlp_dims& d) {
     return s;
 }
 
+namespace {
 inline const void* shard_ptr(const void* base, int i, const Shapes& s) {
     return static_cast<const uint8_t*>(base) + static_cast<size_t>(i) * s.T * s.fi * 2;
 }
+}  // namespace
 
 // With no tokens the weight and bias gradients are zero.
 tpmlp_status zero_weight_grads(const Shapes& s, void* const* dA_shards, void* db1,
@@ -330,7 +312,7 @@ tpmlp_status zero_weight_grads(const Shapes& s, void* const* dA_shards, void* db
 tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* const* X,
                          const void* const* A_shards, const void* b1,
                          const void* const* B_shards, const void* b2, void* const* Z,
-                         const Regions& R, cudaStream_t st) {
+                         const Regions& R, cudaStream_t st, const RowEpilogue* ep) {
     const void* Y = R.y;
     const void* H = R.h;
 
@@ -380,9 +362,16 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
         p.out_part = PART_ROW;
         p.out_rows_per_part = s.Tc;
         p.bias = b2;
+        if (ep) {
+            // Out = residual + Dropout(Z): the residual is read per token chunk
+            for (int j = 0; j < s.chunks; ++j) p.in0[j] = ep->residual[j];
+            p.ld_in = s.h;
+            p.drop = ep->drop;
+        }
         if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
-        TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st,
-                         [&] { return launch_row_fwd(p, st); }));
+        TPMLP_CUDA(timed(TPMLP_KERNEL_ROW_FWD, 1, st, [&] {
+            return ep ? launch_row_fwd_dropout(p, st) : launch_row_fwd(p, st);
+        }));
     }
     return TPMLP_OK;
 }
@@ -530,11 +519,12 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
     return TPMLP_OK;
 }
 
-}  // namespace
+}  // namespace block
 }  // namespace tpmlp
 
 using namespace tpmlp;
 using namespace tpmlp::abi;
+using namespace tpmlp::block;
 
 // =========================================================================================
 TPMLP_API const char* tpmlp_status_string(tpmlp_status s) {
@@ -598,7 +588,7 @@ TPMLP_API tpmlp_status tpmlp_forward(const tpmlp_dims* dims, const void* const* 
     if (s.T == 0) return TPMLP_OK;
     return run_forward(s, dev, X, A_shards, b1, B_shards, b2, Z,
                        regions_of(static_cast<uint8_t*>(workspace), layout_of(*dims)),
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), nullptr);
 }
 
 TPMLP_API tpmlp_status tpmlp_backward(const tpmlp_dims* dims, const void* const* dZ,
@@ -661,7 +651,7 @@ TPMLP_API tpmlp_status tpmlp_forward_recompute(const tpmlp_dims* dims, const voi
     return run_forward(s, dev, X, A_shards, b1, B_shards, b2, Z,
                        recompute_regions(static_cast<uint8_t*>(saved),
                                          static_cast<uint8_t*>(scratch), layout_of(*dims)),
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), nullptr);
 }
 
 TPMLP_API tpmlp_status tpmlp_backward_recompute(const tpmlp_dims* dims, const void* const* dZ,
@@ -802,6 +792,8 @@ TPMLP_API const char* tpmlp_kernel_name(int kind) {
         case TPMLP_KERNEL_LINEAR_FWD: return "linear_fwd";
         case TPMLP_KERNEL_LINEAR_DGRAD: return "linear_dgrad";
         case TPMLP_KERNEL_LINEAR_WGRAD: return "linear_wgrad";
+        case TPMLP_KERNEL_LAYERNORM: return "layernorm";
+        case TPMLP_KERNEL_DROPOUT_BWD: return "dropout_bwd";
     }
     return "unknown";
 }

@@ -15,6 +15,11 @@ Linear layers (``make_linear_inputs``): the same kind of generator draws, in
 this order, X [T, in], W [in, out], b [out], dY [T, out] (dY is the upstream
 gradient of the layer's output), with the same standard deviations.
 
+Sequence-parallel sublayer (``make_sp_inputs``): the block's tensors as
+above (dZ serving as dOut, the sublayer's upstream gradient), then a second
+CPU generator seeded with seed + 0x5EED draws gamma = 1 + 0.1 N(0, 1) and
+beta = 0.02 N(0, 1), both [h], rounded to bf16.
+
 Token rows are ordered sequence-major ([seq, micro-batch] flattened, the usual
 [s, b, h] activation layout), so sequence chunk j is the contiguous row range
 [j*T/n, (j+1)*T/n): a span of sequence positions for every sample.
@@ -184,3 +189,16 @@ def make_linear_inputs(w: LinearWorkload, seed: int = 0) -> dict:
     b = draw((w.out_features,), w.sigma_b)
     dY = draw((w.tokens, w.out_features), 1.0)
     return {"X": X, "W": W, "b": b, "dY": dY}
+
+
+def make_sp_inputs(w: Workload, seed: int = 0) -> dict:
+    """The block's inputs plus the LayerNorm parameters gamma, beta [h] (bf16);
+    "dZ" is the sublayer's upstream gradient dOut."""
+    d = make_inputs(w, seed)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 0x5EED)
+    gamma = (1.0 + 0.1 * torch.randn(w.hidden, generator=g, dtype=torch.float32))
+    beta = 0.02 * torch.randn(w.hidden, generator=g, dtype=torch.float32)
+    d["gamma"] = gamma.to(torch.bfloat16)
+    d["beta"] = beta.to(torch.bfloat16)
+    return d

@@ -54,7 +54,7 @@ def test_status_strings(binding):
     assert binding.tpmlp_status_string(99) == "unknown status"
     assert [binding.tpmlp_kernel_name(k) for k in range(binding.KERNEL_KINDS)] == [
         "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad",
-        "linear_fwd", "linear_dgrad", "linear_wgrad"]
+        "linear_fwd", "linear_dgrad", "linear_wgrad", "layernorm", "dropout_bwd"]
 
 
 def test_workspace_bytes(binding):
@@ -186,6 +186,40 @@ def test_linear_validation_codes(binding):
     assert _lin(binding, rowf, mk(256, 256, 256, 2), nin=[None, FAKE]) == INV
     assert binding.library().tpmlp_row_linear_forward(None, None, None, None, None, None,
                                                       None) == INV
+
+
+def test_sp_workspace_and_validation(binding):
+    mk = binding.make_dims
+    d = mk(16384, 4096, 16384, 8, 8)
+    n = binding.tpmlp_sp_workspace_bytes(d)
+    assert n >= binding.tpmlp_workspace_bytes(d) + 3 * 16384 * 4096 * 2
+    xn, dz = binding.tpmlp_sp_workspace_layout(d)
+    assert binding.tpmlp_workspace_bytes(d) <= xn < dz < n
+    assert binding.tpmlp_sp_workspace_bytes(mk(128, 32768, 1024, 2)) == 0  # h above 16384
+    lib = binding.library()
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    INV, UNS = binding.TPMLP_ERR_INVALID_ARG, binding.TPMLP_ERR_UNSUPPORTED
+    d = mk(256, 256, 1024, 2)
+    two, one = [FAKE, FAKE], [FAKE]
+
+    def fwd(sp, **kw):
+        a = dict(X=one, gamma=FAKE, beta=FAKE, A=two, b1=FAKE, B=two, b2=FAKE, t=2, Out=one,
+                 ws=FAKE)
+        a.update(kw)
+        return lib.tpmlp_sp_forward(ctypes.byref(d), sp, arr(a["X"]), a["gamma"], a["beta"],
+                                    arr(a["A"]), a["b1"], arr(a["B"]), a["b2"], a["t"],
+                                    arr(a["Out"]), a["ws"], None)
+    ok = ctypes.byref(binding.make_sp_params(1e-5, 0.1, 7))
+    assert fwd(None) == INV
+    assert fwd(ctypes.byref(binding.make_sp_params(1e-5, 1.0, 7))) == INV   # p = 1
+    assert fwd(ctypes.byref(binding.make_sp_params(1e-5, -0.1, 7))) == INV
+    assert fwd(ctypes.byref(binding.make_sp_params(-1.0, 0.1, 7))) == INV   # eps < 0
+    assert fwd(ok, gamma=None) == INV
+    assert fwd(ok, beta=FAKE + 2) == UNS
+    assert fwd(ok, t=4) == INV
+    assert lib.tpmlp_sp_backward(ctypes.byref(d), ok, arr(one), arr(one), FAKE, arr(two), arr(two),
+                                 FAKE, arr(one), FAKE, None, arr(two), FAKE, arr(two), FAKE,
+                                 None) == INV  # no dbeta
 
 
 def test_set_timeout_and_profile_args(binding):

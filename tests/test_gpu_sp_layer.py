@@ -1,0 +1,155 @@
+"""Parity of the sequence-parallel sublayer Out = X + Dropout(MLP(LN(X)))
+(LayerNorm and Dropout per token chunk) through the C ABI, against the fp64
+oracle.
+
+Small and ragged layers are compared element by element against the full
+oracle, and the dropout mask exactly (every element the oracle drops is an
+exact zero of the GPU's dZ, and only those).  The 16384 x 4096 sequence-
+parallel workload is compared on sampled rows (Out, dX: each row depends only
+on its own inputs; the mask is taken at the rows' global element indices) and
+sampled columns of the weight gradients (from the oracle's full LN(X) and dZ);
+LayerNorm's dgamma and dbeta are checked element by element at the small
+sizes only.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import gate, sample_indices
+from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
+                                                      make_sp_inputs, row_shards)
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup(gpu):
+    oracle.set_threads(len(os.sched_getaffinity(0)))
+    from tensor_transformer_mlp_gemm_gb300.build import build
+    build()
+    yield
+
+
+def _layer(w, inputs, p, seed=1234):
+    from tensor_transformer_mlp_gemm_gb300.sp import DeviceSPLayer
+    return DeviceSPLayer(w, inputs, eps=EPS, dropout_p=p, seed=seed)
+
+
+def _cat(xs, axis):
+    return torch.cat([x.cpu() for x in xs], dim=axis)
+
+
+def _report(rep):
+    print(" ".join(f"{k}:{v['max_abs'] / v['bound']:.2f}" for k, v in rep.items()))
+
+
+def _run_full(w, p, seed=0):
+    rep = {}
+    inputs = make_sp_inputs(w, seed)
+    lay = _layer(w, inputs, p)
+    lay.step()
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    ref = oracle.sp_layer(inputs["X"], inputs["gamma"], inputs["beta"], EPS,
+                          column_shards(inputs["A"], w.t), inputs["b1"],
+                          row_shards(inputs["B"], w.t), inputs["b2"], p, 1234, dOut=inputs["dZ"])
+    torch.cuda.synchronize()
+    gate("Xn", lay.workspace_tensor("xn").cpu(), ref["Xn"], rep)
+    dz = lay.workspace_tensor("dz").cpu()
+    dropped = ref["keep"] == 0
+    assert torch.all(dz[torch.from_numpy(dropped)] == 0), "kept where the oracle drops"
+    assert torch.all(dz[torch.from_numpy(~dropped)] != 0), "dropped where the oracle keeps"
+    gate("dZ", dz, ref["dZ"], rep)
+    gate("Out", _cat(lay.Out, 0), ref["Out"], rep)
+    gate("dX", _cat(lay.dX, 0), ref["dX"], rep)
+    gate("dgamma", lay.dgamma, ref["dgamma"], rep)
+    gate("dbeta", lay.dbeta, ref["dbeta"], rep)
+    gate("dA", _cat(lay.dA, 1), np.concatenate(ref["dA"], 1), rep)
+    gate("dB", _cat(lay.dB, 0), np.concatenate(ref["dB"], 0), rep)
+    gate("db1", lay.db1, ref["db1"], rep)
+    gate("db2", lay.db2, ref["db2"], rep)
+    _report(rep)
+    return lay, ref
+
+
+@pytest.mark.parametrize("T,h,f,t,chunks,p", [
+    (512, 256, 1024, 4, 4, 0.1),    # four token chunks
+    (333, 264, 1032, 3, 1, 0.2),    # ragged M, N and K tails
+    (256, 2048, 2048, 8, 2, 0.5),   # eight shards, wide rows
+    (128, 256, 1024, 2, 1, 0.0),    # no dropout: Out = X + MLP(LN(X))
+])
+def test_sp_layer_full(T, h, f, t, chunks, p):
+    # weights with the workloads' standard deviation (0.02)
+    _run_full(custom(T, h, f, t, seq_chunks=chunks), p, seed=2)
+
+
+def test_sp_layer_deterministic_and_seeded():
+    w = custom(512, 256, 1024, 4, seq_chunks=4)
+    inputs = make_sp_inputs(w, 3)
+    a, b, c = _layer(w, inputs, 0.1), _layer(w, inputs, 0.1), _layer(w, inputs, 0.1, seed=99)
+    for lay in (a, b, c):
+        lay.step()
+    torch.cuda.synchronize()
+    for x, y in zip(a.Out + a.dX + a.dA + a.dB, b.Out + b.dX + b.dA + b.dB):
+        assert torch.equal(x, y)
+    assert torch.equal(a.dgamma, b.dgamma) and torch.equal(a.dbeta, b.dbeta)
+    assert not torch.equal(a.workspace_tensor("dz"), c.workspace_tensor("dz"))
+
+
+def test_sp_layer_empty_batch_zeroes_gradients():
+    w = custom(0, 64, 256, 2)
+    lay = _layer(w, make_sp_inputs(w, 0), 0.1)
+    for x in lay.dA + lay.dB + [lay.db1, lay.db2, lay.dgamma, lay.dbeta]:
+        x.fill_(7.0)
+    lay.step()
+    torch.cuda.synchronize()
+    for x in lay.dA + lay.dB + [lay.db1, lay.db2, lay.dgamma, lay.dbeta]:
+        assert torch.count_nonzero(x) == 0
+
+
+def test_sp_h4096_sampled():
+    w = WORKLOADS["sp_h4096"]
+    p, seed = 0.1, 1234
+    inputs = make_sp_inputs(w, 0)
+    lay = _layer(w, inputs, p, seed)
+    lay.step()
+    torch.cuda.synchronize()
+    T, h = w.tokens, w.hidden
+    rep = {}
+    X, dOut = inputs["X"], inputs["dZ"]
+    A, B = column_shards(inputs["A"], w.t), row_shards(inputs["B"], w.t)
+    scale = 1.0 / (1.0 - p)
+    rows = sample_indices(T, 8, 31)
+    keep_r = np.stack([oracle.dropout_keep(T, h, p, seed, 0, e0=int(r) * h, count=h)
+                       for r in rows]).astype(np.float64)
+    ln = oracle.layernorm(X[rows], inputs["gamma"], inputs["beta"], EPS)
+    dZ_r = dOut[rows].double().numpy() * keep_r * scale
+    fb = oracle.forward_backward(ln["Xn"], A, inputs["b1"], B, inputs["b2"], dZ_r)
+    Out_r = X[rows].double().numpy() + keep_r * scale * fb["Z"]
+    lnb = oracle.layernorm(X[rows], inputs["gamma"], inputs["beta"], EPS, dXn=fb["dX"])
+    dX_r = lnb["dX"] + dOut[rows].double().numpy()
+    Out = torch.cat(lay.Out, 0)
+    dX = torch.cat(lay.dX, 0)
+    idx = torch.from_numpy(rows).to(Out.device)
+    gate("Out[rows]", Out[idx].cpu(), Out_r, rep)
+    gate("dX[rows]", dX[idx].cpu(), dX_r, rep)
+    # weight-gradient columns from the full LN(X) and dZ
+    Xn = oracle.layernorm(X, inputs["gamma"], inputs["beta"], EPS)["Xn"]
+    keep = oracle.dropout_keep(T, h, p, seed).reshape(T, h)
+    dZ = dOut.double().numpy() * keep * scale
+    del keep
+    cols = sample_indices(w.ffn, 12, 32)
+    c = oracle.cols(Xn, A, inputs["b1"], B, dZ, cols)
+    fi = w.ffn // w.t
+    gate("dA[:,cols]", torch.stack([lay.dA[int(q) // fi][:, int(q) % fi].cpu() for q in cols]),
+         c["dA_cols"], rep)
+    gate("dB[cols,:]", torch.stack([lay.dB[int(q) // fi][int(q) % fi, :].cpu() for q in cols]),
+         c["dB_rows"], rep)
+    gate("db1[cols]", lay.db1.cpu()[cols], c["db1"], rep)
+    gate("db2", lay.db2, oracle.db2(dZ), rep)
+    _report(rep)
