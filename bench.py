@@ -526,8 +526,10 @@ class SpRunner(MlpRunner):
         self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
         self.gemm_flops = 2.0 * T * h * f
         self.colsum_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
-        # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes dX
-        self.ln_bytes = 2 * T * h * 2 + 4 * T * h * 2
+        # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes
+        # dX (the dgamma / dbeta pass re-reads X and dLN(X): not counted, algorithmic bytes only)
+        self.ln_fwd_bytes = 2 * T * h * 2
+        self.ln_bwd_bytes = 4 * T * h * 2
         self.dropout_bytes = 2 * T * h * 2
         self.l2_note = (f"inputs larger than L2 (bf16 weights {2 * h * f * 2 / 1e9:.2f} GB, "
                         f"activations {(3 * T * f + 4 * T * h) * 2 / 1e9:.2f} GB per step)")
@@ -665,7 +667,8 @@ def run_ours(args, torch):
         cs_ms = kms["bias_grad"] / args.steps
         kernels["bias_grad"]["gb_per_s"] = run.colsum_bytes / (cs_ms / 1e3) / 1e9
         kernels["bias_grad"]["frac_of_hbm"] = kernels["bias_grad"]["gb_per_s"] / peaks["hbm_gbs"]
-    for name, attr in (("layernorm", "ln_bytes"), ("dropout_bwd", "dropout_bytes")):
+    for name, attr in (("layernorm_fwd", "ln_fwd_bytes"), ("layernorm_bwd", "ln_bwd_bytes"),
+                       ("dropout_bwd", "dropout_bytes")):
         if name in kernels and hasattr(run, attr):
             per_step = kms[name] / args.steps
             kernels[name]["gb_per_s"] = getattr(run, attr) / (per_step / 1e3) / 1e9

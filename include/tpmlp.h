@@ -380,9 +380,10 @@ enum {
     TPMLP_KERNEL_LINEAR_FWD = 7,  /* linear layers: Y_i = X.W_i + b, Z = sum_i X_i.W_i + b */
     TPMLP_KERNEL_LINEAR_DGRAD = 8,  /* linear layers: dX = sum_i dY_i.W_i^T, dX_i = dZ.W_i^T */
     TPMLP_KERNEL_LINEAR_WGRAD = 9,  /* linear layers: dW_i */
-    TPMLP_KERNEL_LAYERNORM = 10,    /* sequence-parallel sublayer: LN forward, LN backward */
-    TPMLP_KERNEL_DROPOUT_BWD = 11,  /* sequence-parallel sublayer: dZ from dOut and the mask */
-    TPMLP_KERNEL_KINDS = 12
+    TPMLP_KERNEL_LAYERNORM_FWD = 10,  /* sequence-parallel sublayer: LN(X) and row statistics */
+    TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (3 launches) */
+    TPMLP_KERNEL_DROPOUT_BWD = 12,    /* sequence-parallel sublayer: dZ from dOut and the mask */
+    TPMLP_KERNEL_KINDS = 13
 };
 tpmlp_status tpmlp_profile_begin(int capacity);
 int tpmlp_profile_end(double* ms, int* launches, int nkinds);

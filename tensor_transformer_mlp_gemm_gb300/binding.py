@@ -27,7 +27,7 @@ TPMLP_ERR_UNSUPPORTED = 2
 TPMLP_ERR_CUDA = 3
 TPMLP_ERR_TIMEOUT = 4
 
-KERNEL_KINDS = 12
+KERNEL_KINDS = 13
 
 # every symbol include/tpmlp.h declares
 EXPORTED = (

@@ -1,7 +1,9 @@
 // layernorm.cu -- LayerNorm forward/backward and dropout backward of the
 // sequence-parallel sublayer (see layernorm.cuh).  One CTA of 256 threads per
-// token row in the forward pass; each thread holds up to eight 8-element
-// vectors of its row in registers, so X is read once and written once.
+// token row in the forward pass and in the dX pass of the backward; each
+// thread holds up to eight 8-element vectors of its row in registers, so every
+// input is read once and every output written once.  dgamma and dbeta come
+// from a separate column-reduction pass over dXn and X.
 // Reductions run warp-shuffle then one warp over the partial sums, always in
 // the same order.
 #include <cuda_bf16.h>
@@ -140,102 +142,149 @@ __global__ void __launch_bounds__(LN_THREADS) dropout_backward_kernel(const Drop
     *reinterpret_cast<uint4*>(dst) = pack8(f);
 }
 
-// CTA b handles token rows [b * R, (b + 1) * R); dynamic shared memory holds
-// its partial dgamma (first h floats) and dbeta (next h floats), each column
-// owned by one thread.
-__global__ void __launch_bounds__(LN_THREADS) ln_backward_kernel(const LnBackwardParams p,
-                                                                 long long T) {
-    extern __shared__ float acc[];
-    __shared__ float red[LN_THREADS / 32 + 1];
+// Sum of two values over the CTA in one pass (both orders fixed).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
+    constexpr int W = LN_THREADS / 32;
+    a = warp_sum(a);
+    b = warp_sum(b);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) {
+        red[w] = a;
+        red[W + w] = b;
+    }
+    __syncthreads();
+    if (w == 0) {
+        float ta = l < W ? red[l] : 0.0f, tb = l < W ? red[W + l] : 0.0f;
+        ta = warp_sum(ta);
+        tb = warp_sum(tb);
+        if (l == 0) {
+            red[2 * W] = ta;
+            red[2 * W + 1] = tb;
+        }
+    }
+    __syncthreads();
+    return make_float2(red[2 * W], red[2 * W + 1]);
+}
+
+// dX of one token row per CTA:
+//   dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dres,  g = dXn * gamma
+__global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParams p) {
+    __shared__ float red[2 * (LN_THREADS / 32) + 2];
     const int h = p.h;
+    const long long r = blockIdx.x;
+    int j;
+    const long long off = chunk_row(r, p.x.rows, j) * h;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + off;
+    const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(p.dxn[j]) + off;
+    const __nv_bfloat16* dres = static_cast<const __nv_bfloat16*>(p.dres[j]) + off;
+    __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(p.dx[j]) + off;
     const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
-    uint4 gv[LN_MAX_VEC];
+    const float mean = p.mean[r], rs = p.rstd[r];
+    uint4 xv[LN_MAX_VEC], dv[LN_MAX_VEC], rv[LN_MAX_VEC];
+    float sg = 0.0f, sgx = 0.0f;
 #pragma unroll
     for (int i = 0; i < LN_MAX_VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < h) {
-            gv[i] = __ldg(reinterpret_cast<const uint4*>(gm + c));
+            xv[i] = *reinterpret_cast<const uint4*>(x + c);
+            dv[i] = *reinterpret_cast<const uint4*>(dy + c);
+            rv[i] = *reinterpret_cast<const uint4*>(dres + c);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < h) {
+            float xf[8], df[8], gf[8];
+            unpack8(xv[i], xf);
+            unpack8(dv[i], df);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gm + c)), gf);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                acc[c + k] = 0.0f;
-                acc[h + c + k] = 0.0f;
+                const float g = df[k] * gf[k];
+                sg += g;
+                sgx += g * (xf[k] - mean) * rs;
             }
         }
     }
-    const long long r0 = static_cast<long long>(blockIdx.x) * p.rows_per_block;
+    const float2 sums = block_sum2(sg, sgx, red);
+    const float mg = sums.x / static_cast<float>(h), mgx = sums.y / static_cast<float>(h);
+#pragma unroll
+    for (int i = 0; i < LN_MAX_VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < h) {
+            float xf[8], df[8], gf[8], rf[8], o[8];
+            unpack8(xv[i], xf);
+            unpack8(dv[i], df);
+            unpack8(rv[i], rf);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gm + c)), gf);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                o[k] = rs * (df[k] * gf[k] - mg - (xf[k] - mean) * rs * mgx) + rf[k];
+            *reinterpret_cast<uint4*>(dx + c) = pack8(o);
+        }
+    }
+}
+
+// dgamma / dbeta partial column sums: CTA = a 64-column strip x 32 row slots
+// over the rows of split blockIdx.y; thread (slot, vec) accumulates columns
+// vec*8 .. vec*8+7 of rows slot, slot + 32, ...; the slots are then added in
+// order through shared memory.  part[split][0][c] = sum dXn * xhat,
+// part[split][1][c] = sum dXn.
+__global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackwardParams p,
+                                                                   long long T) {
+    constexpr int COLS = 64;
+    __shared__ float red[2][32][COLS + 1];
+    const int h = p.h;
+    const int vec = threadIdx.x & 7, slot = threadIdx.x >> 3;
+    const int col = blockIdx.x * COLS + vec * 8;
+    const long long r0 = static_cast<long long>(blockIdx.y) * p.rows_per_block;
     const long long r1 = r0 + p.rows_per_block < T ? r0 + p.rows_per_block : T;
-    for (long long r = r0; r < r1; ++r) {
-        int j;
-        const long long rr = chunk_row(r, p.x.rows, j);
-        const long long off = rr * h;
-        const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + off;
-        const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(p.dxn[j]) + off;
-        const __nv_bfloat16* dres = static_cast<const __nv_bfloat16*>(p.dres[j]) + off;
-        __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(p.dx[j]) + off;
-        const float mean = p.mean[r], rs = p.rstd[r];
-        uint4 xv[LN_MAX_VEC], dv[LN_MAX_VEC];
-        float sg = 0.0f, sgx = 0.0f;
+    float ag[8], ab[8];
 #pragma unroll
-        for (int i = 0; i < LN_MAX_VEC; ++i) {
-            const int c = (threadIdx.x + i * LN_THREADS) * 8;
-            if (c < h) {
-                xv[i] = *reinterpret_cast<const uint4*>(x + c);
-                dv[i] = *reinterpret_cast<const uint4*>(dy + c);
-                float xf[8], df[8], gf[8];
-                unpack8(xv[i], xf);
-                unpack8(dv[i], df);
-                unpack8(gv[i], gf);
+    for (int k = 0; k < 8; ++k) ag[k] = ab[k] = 0.0f;
+    if (col < h) {
+        for (long long r = r0 + slot; r < r1; r += 32) {
+            int j;
+            const long long off = chunk_row(r, p.x.rows, j) * h + col;
+            float xf[8], df[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(
+                        static_cast<const __nv_bfloat16*>(p.x.in[j]) + off)), xf);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(
+                        static_cast<const __nv_bfloat16*>(p.dxn[j]) + off)), df);
+            const float mean = __ldg(p.mean + r), rs = __ldg(p.rstd + r);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float g = df[k] * gf[k];
-                    sg += g;
-                    sgx += g * (xf[k] - mean) * rs;
-                }
-            }
-        }
-        const float mg = block_sum(sg, red) / static_cast<float>(h);
-        const float mgx = block_sum(sgx, red) / static_cast<float>(h);
-#pragma unroll
-        for (int i = 0; i < LN_MAX_VEC; ++i) {
-            const int c = (threadIdx.x + i * LN_THREADS) * 8;
-            if (c < h) {
-                float xf[8], df[8], gf[8], rf[8], o[8];
-                unpack8(xv[i], xf);
-                unpack8(dv[i], df);
-                unpack8(gv[i], gf);
-                unpack8(*reinterpret_cast<const uint4*>(dres + c), rf);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float xh = (xf[k] - mean) * rs;
-                    o[k] = rs * (df[k] * gf[k] - mg - xh * mgx) + rf[k];
-                    acc[c + k] += df[k] * xh;
-                    acc[h + c + k] += df[k];
-                }
-                *reinterpret_cast<uint4*>(dx + c) = pack8(o);
+            for (int k = 0; k < 8; ++k) {
+                ag[k] += df[k] * ((xf[k] - mean) * rs);
+                ab[k] += df[k];
             }
         }
     }
-    float* part = p.part + static_cast<size_t>(blockIdx.x) * 2 * h;
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
-        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+    for (int k = 0; k < 8; ++k) {
+        red[0][slot][vec * 8 + k] = ag[k];
+        red[1][slot][vec * 8 + k] = ab[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * COLS) {
+        const int which = threadIdx.x / COLS, cc = threadIdx.x % COLS;
+        const int c = blockIdx.x * COLS + cc;
         if (c < h) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                part[c + k] = acc[c + k];
-                part[h + c + k] = acc[h + c + k];
-            }
+            float s = 0.0f;
+            for (int k = 0; k < 32; ++k) s += red[which][k][cc];
+            p.part[(static_cast<size_t>(blockIdx.y) * 2 + which) * h + c] = s;
         }
     }
 }
 
 // dgamma[c] = sum_b part[b][0][c], dbeta[c] = sum_b part[b][1][c], b in order
-__global__ void ln_finish_kernel(const float* part, int blocks, int h, float* dgamma,
+__global__ void ln_finish_kernel(const float* part, int splits, int h, float* dgamma,
                                  float* dbeta) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= h) return;
     float g = 0.0f, b = 0.0f;
-    for (int k = 0; k < blocks; ++k) {
+    for (int k = 0; k < splits; ++k) {
         g += part[static_cast<size_t>(k) * 2 * h + c];
         b += part[static_cast<size_t>(k) * 2 * h + h + c];
     }
@@ -260,18 +309,18 @@ cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T,
     return cudaGetLastError();
 }
 
-cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int blocks, float* dgamma,
+cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st) {
-    const size_t smem = 2 * static_cast<size_t>(p.h) * sizeof(float);
-    // per device; a host-side call, cheap enough to repeat
-    cudaError_t e = cudaFuncSetAttribute(ln_backward_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(2 * LN_MAX_H * sizeof(float)));
+    if (T > 0) {
+        ln_dx_kernel<<<static_cast<unsigned>(T), LN_THREADS, 0, st>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid(static_cast<unsigned>((p.h + 63) / 64), static_cast<unsigned>(splits));
+    ln_param_grad_kernel<<<grid, LN_THREADS, 0, st>>>(p, T);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    ln_backward_kernel<<<blocks, LN_THREADS, smem, st>>>(p, T);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    ln_finish_kernel<<<(p.h + 255) / 256, 256, 0, st>>>(p.part, blocks, p.h, dgamma, dbeta);
+    ln_finish_kernel<<<(p.h + 255) / 256, 256, 0, st>>>(p.part, splits, p.h, dgamma, dbeta);
     return cudaGetLastError();
 }
 

@@ -6,9 +6,9 @@
 //                     kept for the backward pass
 //   dropout_backward: dZ = keep ? dOut / (1 - p) : 0 (the forward's mask)
 //   ln_backward:      dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dOut,
-//                     g = dXn * gamma, plus per-CTA partial column sums of
-//                     dXn * xhat and dXn; ln_finish sums them in a fixed order
-//                     into dgamma and dbeta (no atomics anywhere).
+//                     g = dXn * gamma (one CTA per token row), then dgamma =
+//                     sum dXn * xhat and dbeta = sum dXn as column sums over
+//                     row splits, added in split order (no atomics anywhere).
 // All three are bound by HBM traffic.
 #pragma once
 
@@ -56,26 +56,34 @@ struct LnBackwardParams {
     const void* gamma;           // bf16 [h]
     const float* mean;
     const float* rstd;
-    float* part;                 // fp32 [blocks][2][h] partial dgamma, dbeta
+    float* part;                 // fp32 [splits][2][h] partial dgamma, dbeta
     int h;
-    long long rows_per_block;
+    long long rows_per_block;    // rows per split of the dgamma / dbeta pass
 };
 
-// Bytes of partial sums ln_backward needs for `blocks` CTAs.
-inline size_t ln_partial_bytes(int blocks, long long h) {
-    return static_cast<size_t>(blocks) * 2 * static_cast<size_t>(h) * sizeof(float);
+constexpr int LN_MAX_SPLITS = 64;
+
+// Bytes of partial sums the dgamma / dbeta pass needs.
+inline size_t ln_partial_bytes(long long h) {
+    return static_cast<size_t>(LN_MAX_SPLITS) * 2 * static_cast<size_t>(h) * sizeof(float);
 }
-// CTAs ln_backward uses for T rows on a GPU with sm_count SMs.
-inline int ln_backward_blocks(long long T, int sm_count) {
-    const long long b = 2LL * sm_count;
-    return static_cast<int>(T < b ? (T > 0 ? T : 1) : b);
+// Row splits of the dgamma / dbeta pass: enough 64-column CTAs to cover the
+// GPU about four times, at least 256 rows per split.
+inline int ln_param_splits(long long T, long long h, int sm_count) {
+    const long long strips = (h + 63) / 64;
+    long long s = (4LL * sm_count + strips - 1) / strips;
+    const long long by_rows = T / 256 > 0 ? T / 256 : 1;
+    if (s > by_rows) s = by_rows;
+    if (s > LN_MAX_SPLITS) s = LN_MAX_SPLITS;
+    return static_cast<int>(s < 1 ? 1 : s);
 }
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st);
 cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, int sm_count,
                                     cudaStream_t st);
-// Two launches: ln_backward over `blocks` CTAs, then the fixed-order finish.
-cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int blocks, float* dgamma,
+// Three launches: dX per token row, the dgamma / dbeta partial column sums
+// over `splits` row splits, and their fixed-order finish.
+cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st);
 
 }  // namespace tpmlp

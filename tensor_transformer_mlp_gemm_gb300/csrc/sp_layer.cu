@@ -37,10 +37,6 @@ struct SpLayout {
     size_t xn, mean, rstd, dz, dxn, part, total;
 };
 
-// The partial sums are sized for the largest CTA count any GPU of this kind
-// uses (2 x 160 SMs), so the size does not depend on the device.
-constexpr int kMaxLnBlocks = 320;
-
 SpLayout sp_layout_of(const tpmlp_dims& d) {
     SpLayout L;
     L.blk = layout_of(d);
@@ -52,7 +48,7 @@ SpLayout sp_layout_of(const tpmlp_dims& d) {
     L.dz = L.rstd + row;
     L.dxn = L.dz + act;
     L.part = L.dxn + act;
-    L.total = L.part + align256(ln_partial_bytes(kMaxLnBlocks, d.hidden));
+    L.total = L.part + align256(ln_partial_bytes(d.hidden));
     return L;
 }
 
@@ -145,7 +141,8 @@ TPMLP_API tpmlp_status tpmlp_sp_forward(const tpmlp_dims* dims, const tpmlp_sp_p
     ln.rstd = reinterpret_cast<float*>(ws + L.rstd);
     ln.h = s.h;
     ln.eps = sp->eps;
-    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM, 1, st, [&] { return launch_ln_forward(ln, s.T, st); }));
+    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_FWD, 1, st,
+                     [&] { return launch_ln_forward(ln, s.T, st); }));
 
     RowEpilogue ep;
     ep.residual = X;
@@ -223,11 +220,10 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_
     lb.rstd = reinterpret_cast<const float*>(ws + L.rstd);
     lb.part = reinterpret_cast<float*>(ws + L.part);
     lb.h = s.h;
-    int blocks = ln_backward_blocks(s.T, dev->sm_count);
-    if (blocks > kMaxLnBlocks) blocks = kMaxLnBlocks;
-    lb.rows_per_block = (s.T + blocks - 1) / blocks;
-    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM, 2, st, [&] {
-        return launch_ln_backward(lb, s.T, blocks, static_cast<float*>(dgamma),
+    const int splits = ln_param_splits(s.T, s.h, dev->sm_count);
+    lb.rows_per_block = (s.T + splits - 1) / splits;
+    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_BWD, 3, st, [&] {
+        return launch_ln_backward(lb, s.T, splits, static_cast<float*>(dgamma),
                                   static_cast<float*>(dbeta), st);
     }));
     return TPMLP_OK;

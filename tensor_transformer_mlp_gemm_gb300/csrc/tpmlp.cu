@@ -792,7 +792,8 @@ TPMLP_API const char* tpmlp_kernel_name(int kind) {
         case TPMLP_KERNEL_LINEAR_FWD: return "linear_fwd";
         case TPMLP_KERNEL_LINEAR_DGRAD: return "linear_dgrad";
         case TPMLP_KERNEL_LINEAR_WGRAD: return "linear_wgrad";
-        case TPMLP_KERNEL_LAYERNORM: return "layernorm";
+        case TPMLP_KERNEL_LAYERNORM_FWD: return "layernorm_fwd";
+        case TPMLP_KERNEL_LAYERNORM_BWD: return "layernorm_bwd";
         case TPMLP_KERNEL_DROPOUT_BWD: return "dropout_bwd";
     }
     return "unknown";

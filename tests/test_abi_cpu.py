@@ -54,7 +54,8 @@ def test_status_strings(binding):
     assert binding.tpmlp_status_string(99) == "unknown status"
     assert [binding.tpmlp_kernel_name(k) for k in range(binding.KERNEL_KINDS)] == [
         "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad",
-        "linear_fwd", "linear_dgrad", "linear_wgrad", "layernorm", "dropout_bwd"]
+        "linear_fwd", "linear_dgrad", "linear_wgrad", "layernorm_fwd", "layernorm_bwd",
+        "dropout_bwd"]
 
 
 def test_workspace_bytes(binding):
