@@ -66,6 +66,8 @@ def parse_args():
                     help="selective recompute: keep only Y between passes, rebuild H in backward")
     ap.add_argument("--split-min-kblocks", type=int, default=None,
                     help="tail-split depth threshold of the GEMMs (0 = off; library default 128)")
+    ap.add_argument("--head-prefetch", type=int, default=None,
+                    help="K steps of the next tile the GEMMs prefetch into L2 (library default)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -601,6 +603,8 @@ def run_ours(args, torch):
     torch.cuda.set_device(dev)
     if args.split_min_kblocks is not None:
         binding.tpmlp_set_split_min_kblocks(args.split_min_kblocks)
+    if args.head_prefetch is not None:
+        binding.tpmlp_set_head_prefetch(args.head_prefetch)
     if is_linear(args):
         run = LinearRunner(args, dev)
     elif args.sp_layer:

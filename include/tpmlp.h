@@ -323,6 +323,15 @@ tpmlp_status tpmlp_sync_check(void* stream);
  * turns it off.  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_split_min_kblocks(int kblocks);
 
+/* Head prefetch of the GEMMs: when a CTA pair starts a tile, it asks L2 for
+ * the first `kblocks` 64-deep K steps of its next tile's operands, a whole
+ * tile ahead of the loads that use them.  Helps GEMMs with short K ranges per
+ * tile (the weight gradients, K = tokens), whose tile starts otherwise wait for
+ * data fetched from DRAM; costs one extra TMA instruction per prefetched box.
+ * 0 turns it off; 0..64, else TPMLP_ERR_INVALID_ARG.  Results do not depend on
+ * it.  Affects launches enqueued after the call. */
+tpmlp_status tpmlp_set_head_prefetch(int kblocks);
+
 /* Upper bound, in nanoseconds, on any single wait inside a kernel of this
  * library (default 2e9).  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);

@@ -39,6 +39,7 @@ EXPORTED = (
     "tpmlp_linear_workspace_bytes", "tpmlp_column_linear_forward", "tpmlp_column_linear_backward",
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
     "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
+    "tpmlp_set_head_prefetch",
 )
 
 
@@ -93,6 +94,8 @@ _lib.tpmlp_sync_check.restype = ctypes.c_int
 _lib.tpmlp_sync_check.argtypes = [_vp]
 _lib.tpmlp_set_split_min_kblocks.restype = ctypes.c_int
 _lib.tpmlp_set_split_min_kblocks.argtypes = [ctypes.c_int]
+_lib.tpmlp_set_head_prefetch.restype = ctypes.c_int
+_lib.tpmlp_set_head_prefetch.argtypes = [ctypes.c_int]
 _lib.tpmlp_set_wait_timeout_ns.restype = ctypes.c_int
 _lib.tpmlp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.tpmlp_selftest_stalled_gemm.restype = ctypes.c_int
@@ -235,6 +238,10 @@ def tpmlp_sync_check(stream=None) -> int:
 
 def tpmlp_set_split_min_kblocks(kblocks: int) -> None:
     _check(_lib.tpmlp_set_split_min_kblocks(int(kblocks)), "tpmlp_set_split_min_kblocks")
+
+
+def tpmlp_set_head_prefetch(kblocks: int) -> None:
+    _check(_lib.tpmlp_set_head_prefetch(int(kblocks)), "tpmlp_set_head_prefetch")
 
 
 def tpmlp_set_wait_timeout_ns(ns: int) -> None:

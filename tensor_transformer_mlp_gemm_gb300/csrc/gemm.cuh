@@ -238,6 +238,23 @@ __device__ __forceinline__ void load_operand(const OperandCursor& c, int kc, uin
     }
 }
 
+// The same boxes as load_operand, prefetched into L2 only.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void prefetch_operand(const OperandCursor& c, int kc) {
+    const int k = c.kbase + kc;
+    if constexpr (!MN) {
+        ptx::tma_prefetch_2d(c.map, k, c.r);
+    } else {
+        if (c.mn3d) {
+            ptx::tma_prefetch_3d(c.map, 0, k, c.r / MN_CHUNK);
+        } else {
+#pragma unroll
+            for (int j = 0; j < ROWS / MN_CHUNK; ++j)
+                ptx::tma_prefetch_2d(c.map, c.r + j * MN_CHUNK, k);
+        }
+    }
+}
+
 // Descriptor of the 16-wide K slice `kk` (0..3) of a stage's operand tile.
 //   K-major:  rows of 128 B, 8-row swizzle atoms stacked every 1024 B (SBO);
 //             the K slice starts 32 B further along the row.
@@ -446,6 +463,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                                                   g, seg, a_row, p.K, p.a_mn3d);
                 OperandCursor cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps,
                                                   g, seg, b_row, p.K, p.b_mn3d);
+                // head prefetch: the first K steps of this pair's next tile go to L2
+                // now, a whole tile ahead of their loads (short-K GEMMs, where
+                // every tile start would otherwise wait for first-touch data)
+                if (p.head_prefetch > 0 && !p.stall_producer) {
+                    WorkItem nx;
+                    if (work_item(p, cluster, nclusters, j + 1, nk, nx)) {
+                        int ng, nm0, nn0;
+                        decode_tile(p, nx.tile, ng, nm0, nn0);
+                        const int nseg = nx.kbeg / kblocks;
+                        const int nkb = nx.kbeg - nseg * kblocks;
+                        const OperandCursor pa =
+                            operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps, ng,
+                                           nseg, nm0 + rank * BM, p.K, p.a_mn3d);
+                        const OperandCursor pb =
+                            operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, ng,
+                                           nseg, nn0 + rank * B_ROWS, p.K, p.b_mn3d);
+                        const int stop = min(nkb + p.head_prefetch, kblocks);
+                        for (int q = nkb; q < stop && nseg * kblocks + q < nx.kend; ++q) {
+                            prefetch_operand<A_MN, BM>(pa, q * BK);
+                            prefetch_operand<B_MN, B_ROWS>(pb, q * BK);
+                        }
+                    }
+                }
                 for (int kk = it.kbeg; kk < it.kend; ++kk) {
                     if (kb == kblocks) {
                         kb = 0;
@@ -588,6 +628,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             }
         };
 
+        // fp32 outputs (the weight gradients: short K, 128 KB per CTA per tile)
+        // are stored paced over about half the time the next tile's MMAs take
+        // (measured as the gap between accumulator hand-overs): stored in one
+        // burst, all pairs' stores would meet the next tiles' first loads
+        uint64_t t_prev_full = 0;
         int lt = 0;
         WorkItem it;
         for (int j = 0; work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
@@ -604,6 +649,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             if (*epi_fail) break;
             __syncwarp();
             ptx::tc_fence_after();
+            unsigned pace_ns = 0;
+            if constexpr (EPI == EPI_F32) {
+                const uint64_t t_now = ptx::globaltimer_ns();
+                if (t_prev_full != 0 && it.unit < 0) {
+                    const uint64_t gap = t_now - t_prev_full;  // ~ one tile of MMAs
+                    const uint64_t ns = gap * 9 / 128;         // x 7 chunks ~ half of it
+                    pace_ns = static_cast<unsigned>(ns < 4000 ? ns : 4000);
+                }
+                t_prev_full = t_now;
+            }
             // output map and row coordinate of this warp's 32 rows
             int part = g;
             int y0 = m0 + quarter * 32;
@@ -634,6 +689,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
                     epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                    if (pace_ns && c > 0) __nanosleep(pace_ns);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                 }
                 ptx::tc_fence_before();

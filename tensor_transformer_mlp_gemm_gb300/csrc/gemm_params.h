@@ -81,6 +81,8 @@ struct GemmParams {
     int splits;             // K splits per leftover tile
     int units;              // leftover tiles x splits
     int split_min_kblocks;  // split only when a tile has at least this many K steps
+    int head_prefetch;      // at a tile's start, prefetch this many K steps of the next
+                            // tile's operands into L2 (0 = off)
     CUtensorMap part_map;   // fp32 [MAX_SPLIT_UNITS * CLUSTER_M, BN] partial tiles
     const float* partial;   // same buffer, for the summing loads
     int* counters;          // [MAX_SPLIT_UNITS][2] arrivals per leftover tile and CTA

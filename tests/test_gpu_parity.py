@@ -218,3 +218,26 @@ def test_rejects_bad_arguments_on_device():
     with pytest.raises(binding.TpmlpError) as e:
         binding.tpmlp_forward(blk.dims, blk.X, blk.A, blk.b1, blk.B, blk.b2, 2, blk.Z, off)
     assert e.value.status == binding.TPMLP_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T,h,f,t,chunks", [
+    (333, 264, 1032, 3, 1),    # ragged tails: prefetched boxes reach past the tensor edges
+    (512, 256, 1024, 4, 4),    # token chunks
+])
+def test_head_prefetch_full_and_bitwise(T, h, f, t, chunks):
+    """L2 prefetches of the next tile's first K steps never change a result."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    w = custom(T, h, f, t, sigma_w=0.05, seq_chunks=chunks)
+    inputs = make_inputs(w, 14)
+    plain = _block(w, inputs)
+    plain.step()
+    binding.tpmlp_set_head_prefetch(4)
+    try:
+        pf = _run_full(w, seed=14)
+    finally:
+        binding.tpmlp_set_head_prefetch(0)
+    torch.cuda.synchronize()
+    _assert_bitwise(pf.Z, plain.Z, "Z")
+    _assert_bitwise(pf.dX, plain.dX, "dX")
+    _assert_bitwise(pf.dA, plain.dA, "dA")
+    _assert_bitwise(pf.dB, plain.dB, "dB")
