@@ -313,10 +313,37 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* buf, int r, const float 
     }
 }
 
-// Elementwise work on one thread's 32 values: row m, columns [n, n + 32).
+// Epilogues that read a second input per output element (the saved Y of the
+// dGeLU epilogues, the residual of the dropout epilogue).
+template <int EPI>
+struct EpiReadsIn0 {
+    static constexpr bool value =
+        EPI == EPI_DGELU || EPI == EPI_DGELU_H || EPI == EPI_BIAS_DROP_RES;
+};
+
+// That input for one thread's 32 values (row `row` of part `part`, columns
+// [n, n + 32)), as four 16-byte vectors.  Issued ahead of the accumulator
+// chunk it belongs to, so its latency overlaps the previous chunk's work.
+template <int EPI>
+__device__ __forceinline__ void load_in0(const GemmParams& p, int part, long long row, int m,
+                                         int n, uint4 (&u)[4]) {
+    if constexpr (EpiReadsIn0<EPI>::value) {
+        if (m < p.M && n < p.N) {
+            const __nv_bfloat16* src =
+                static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n + 8 * q < p.N) u[q] = *reinterpret_cast<const uint4*>(src + 8 * q);
+        }
+    }
+}
+
+// Elementwise work on one thread's 32 values: row m, columns [n, n + 32);
+// `in` holds the second input (load_in0) for the epilogues that read one.
 template <int EPI>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int part, long long row,
-                                              int m, int n, float (&x)[32], float (&x2)[32]) {
+                                              int m, int n, float (&x)[32], float (&x2)[32],
+                                              const uint4 (&in)[4]) {
     if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS || EPI == EPI_BIAS_DROP_RES) {
         const __nv_bfloat16* b =
             static_cast<const __nv_bfloat16*>(p.bias) + n + g * p.bias_group_stride;
@@ -350,13 +377,11 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
                     x[4 * q + j] = keep ? x[4 * q + j] * p.drop.scale : 0.0f;
                 }
             }
-            const __nv_bfloat16* res =
-                static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (n + 8 * q < p.N) {
                     float rf[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(res + 8 * q), rf);
+                    unpack_bf16x8(in[q], rf);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) x[8 * q + j] += rf[j];
                 }
@@ -365,13 +390,11 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
     }
     if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
         if (m < p.M) {
-            const __nv_bfloat16* y =
-                static_cast<const __nv_bfloat16*>(p.in0[part]) + row * p.ld_in + n;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (n + 8 * q < p.N) {
                     float yf[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4*>(y + 8 * q), yf);
+                    unpack_bf16x8(in[q], yf);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         x[8 * q + j] *= gelu_grad_f(yf[j]);
@@ -641,6 +664,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const int m0 = mp + rank * BM;  // this CTA's first row
             const int acc = lt & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
+            // output map and row coordinate of this warp's 32 rows
+            int part = g;
+            int y0 = m0 + quarter * 32;
+            if (p.out_part == PART_ROW && m0 < p.M) {
+                part = m0 / p.out_rows_per_part;
+                y0 -= part * p.out_rows_per_part;
+            }
+            const int m = m0 + row;
+            const long long in_row = static_cast<long long>(y0) + lane;
+            // the second input of the first chunk is read before the accumulator is ready
+            uint4 pre[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                            make_uint4(0, 0, 0, 0)};
+            if (it.unit < 0) load_in0<EPI>(p, part, in_row, m, n0, pre);
             const bool ok = wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag, p,
                                          ERR_EPILOGUE);
             // all four epilogue warps give up together (they share named barriers)
@@ -659,15 +695,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
                 t_prev_full = t_now;
             }
-            // output map and row coordinate of this warp's 32 rows
-            int part = g;
-            int y0 = m0 + quarter * 32;
-            if (p.out_part == PART_ROW && m0 < p.M) {
-                part = m0 / p.out_rows_per_part;
-                y0 -= part * p.out_rows_per_part;
-            }
-            const int m = m0 + row;
-            const long long in_row = static_cast<long long>(y0) + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             const CUtensorMap* out1 = &p.out_map[part];
@@ -682,13 +709,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
+                    uint4 cur[4] = {pre[0], pre[1], pre[2], pre[3]};
+                    if (c + 1 < BN / EPI_CHUNK)  // next chunk's second input, in flight meanwhile
+                        load_in0<EPI>(p, part, in_row, m, n0 + (c + 1) * EPI_CHUNK, pre);
                     ptx::tmem_ld_wait();
                     const int n = n0 + c * EPI_CHUNK;
                     if (n >= p.N || m0 >= p.M) continue;  // outside the tensor (warp-uniform)
                     float x[32], x2[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
-                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, cur);
                     if (pace_ns && c > 0) __nanosleep(pace_ns);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                 }
@@ -752,7 +782,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             x[4 * q + 3] += f.w;
                         }
                     }
-                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2);
+                    uint4 in[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                   make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+                    load_in0<EPI>(p, part, in_row, m, n, in);
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, in);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                 }
                 if (warp == 2 && lane == 0) p.counters[slot] = 0;  // ready for the next launch
