@@ -68,6 +68,9 @@ def parse_args():
                     help="tail-split depth threshold of the GEMMs (0 = off; library default 128)")
     ap.add_argument("--head-prefetch", type=int, default=None,
                     help="K steps of the next tile the GEMMs prefetch into L2 (library default)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph (the per-kernel "
+                         "times then come from eager steps run after the timed region)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -622,21 +625,45 @@ def run_ours(args, torch):
     st = binding.tpmlp_sync_check(stream)
     if st != binding.TPMLP_OK:
         raise RuntimeError(f"warm-up failed: {binding.tpmlp_status_string(st)}")
+    graph = None
+    if args.graph:
+        # one whole step captured once; every timed step is a replay of it
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run.step(torch.cuda.current_stream(dev))
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
     barrier(dist, torch)
     sampler = ClockSampler(gpu_selector(torch, local))
     sampler.start()
     time.sleep(0.5)
-    binding.tpmlp_profile_begin(16 * args.steps + 16)
+    if graph is None:
+        binding.tpmlp_profile_begin(16 * args.steps + 16)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(dist, torch)
     e0.record(stream)
     for _ in range(args.steps):
-        run.step(stream)
+        if graph is None:
+            run.step(stream)
+        else:
+            graph.replay()
     e1.record(stream)
     barrier(dist, torch)
-    kms, kcount = binding.tpmlp_profile_end()
     clocks = sampler.stop()
+    if graph is None:
+        kms, kcount = binding.tpmlp_profile_end()
+    else:
+        # per-kernel times from eager steps after the timed region
+        prof_steps = min(args.steps, 50)
+        binding.tpmlp_profile_begin(16 * prof_steps + 16)
+        for _ in range(prof_steps):
+            run.step(stream)
+        kms, kcount = binding.tpmlp_profile_end()
+        scale = args.steps / prof_steps
+        kms = {k: v * scale for k, v in kms.items()}
+        kcount = {k: int(round(v * scale)) for k, v in kcount.items()}
     st = binding.tpmlp_sync_check(stream)
     if st != binding.TPMLP_OK:
         raise RuntimeError(f"timed loop failed: {binding.tpmlp_status_string(st)}")
@@ -770,6 +797,11 @@ def run_ours(args, torch):
                                      "source": peak_src},
                 "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks, "gpu_launches": int(sum(kcount.values())),
+                "cuda_graph": bool(args.graph),
+                "kernel_timing": ("CUDA events around each launch inside the timed region"
+                                  if graph is None else
+                                  "CUDA events around each launch of eager steps run after the "
+                                  "timed region (replays of the captured step carry no events)"),
                 "gpu_launches_per_step": launches_per_step}
         print(json.dumps(line), flush=True)
     if dist is not None:
