@@ -62,6 +62,9 @@ __device__ __forceinline__ long long chunk_row(long long r, long long rows, int&
     return r - static_cast<long long>(j) * rows;
 }
 
+// VEC = 8-element vectors per thread (h <= VEC * 8 * LN_THREADS): the row's
+// registers are sized to the row, so narrow rows keep more CTAs per SM.
+template <int VEC>
 __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardParams p) {
     __shared__ float red[LN_THREADS / 32 + 1];
     const long long r = blockIdx.x;
@@ -69,10 +72,10 @@ __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardP
     const long long rr = chunk_row(r, p.x.rows, j);
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + rr * p.h;
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y[j]) + rr * p.h;
-    uint4 v[LN_MAX_VEC];
+    uint4 v[VEC];
     float s = 0.0f;
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < p.h) {
             v[i] = *reinterpret_cast<const uint4*>(x + c);
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardP
     const float mean = block_sum(s, red) / static_cast<float>(p.h);
     float q = 0.0f;
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < p.h) {
             float f[8];
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardP
     const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
     const __nv_bfloat16* bt = static_cast<const __nv_bfloat16*>(p.beta);
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < p.h) {
             float f[8], g[8], b[8], o[8];
@@ -169,6 +172,7 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
 
 // dX of one token row per CTA:
 //   dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dres,  g = dXn * gamma
+template <int VEC>
 __global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParams p) {
     __shared__ float red[2 * (LN_THREADS / 32) + 2];
     const int h = p.h;
@@ -181,19 +185,18 @@ __global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParam
     __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(p.dx[j]) + off;
     const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
     const float mean = p.mean[r], rs = p.rstd[r];
-    uint4 xv[LN_MAX_VEC], dv[LN_MAX_VEC], rv[LN_MAX_VEC];
+    uint4 xv[VEC], dv[VEC];
     float sg = 0.0f, sgx = 0.0f;
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < h) {
             xv[i] = *reinterpret_cast<const uint4*>(x + c);
             dv[i] = *reinterpret_cast<const uint4*>(dy + c);
-            rv[i] = *reinterpret_cast<const uint4*>(dres + c);
         }
     }
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < h) {
             float xf[8], df[8], gf[8];
@@ -211,13 +214,13 @@ __global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParam
     const float2 sums = block_sum2(sg, sgx, red);
     const float mg = sums.x / static_cast<float>(h), mgx = sums.y / static_cast<float>(h);
 #pragma unroll
-    for (int i = 0; i < LN_MAX_VEC; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int c = (threadIdx.x + i * LN_THREADS) * 8;
         if (c < h) {
             float xf[8], df[8], gf[8], rf[8], o[8];
             unpack8(xv[i], xf);
             unpack8(dv[i], df);
-            unpack8(rv[i], rf);
+            unpack8(*reinterpret_cast<const uint4*>(dres + c), rf);
             unpack8(__ldg(reinterpret_cast<const uint4*>(gm + c)), gf);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -292,11 +295,23 @@ __global__ void ln_finish_kernel(const float* part, int splits, int h, float* dg
     dbeta[c] = b;
 }
 
+// Vectors per thread for rows of h elements: the smallest of 1, 2, 4, 8 that covers h.
+int ln_vec(int h) {
+    const int v = (h + 8 * LN_THREADS - 1) / (8 * LN_THREADS);
+    return v <= 1 ? 1 : v <= 2 ? 2 : v <= 4 ? 4 : 8;
+}
+
 }  // namespace
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
-    ln_forward_kernel<<<static_cast<unsigned>(T), LN_THREADS, 0, st>>>(p);
+    const unsigned grid = static_cast<unsigned>(T);
+    switch (ln_vec(p.h)) {
+        case 1: ln_forward_kernel<1><<<grid, LN_THREADS, 0, st>>>(p); break;
+        case 2: ln_forward_kernel<2><<<grid, LN_THREADS, 0, st>>>(p); break;
+        case 4: ln_forward_kernel<4><<<grid, LN_THREADS, 0, st>>>(p); break;
+        default: ln_forward_kernel<8><<<grid, LN_THREADS, 0, st>>>(p); break;
+    }
     return cudaGetLastError();
 }
 
@@ -312,7 +327,13 @@ cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T,
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st) {
     if (T > 0) {
-        ln_dx_kernel<<<static_cast<unsigned>(T), LN_THREADS, 0, st>>>(p);
+        const unsigned grid = static_cast<unsigned>(T);
+        switch (ln_vec(p.h)) {
+            case 1: ln_dx_kernel<1><<<grid, LN_THREADS, 0, st>>>(p); break;
+            case 2: ln_dx_kernel<2><<<grid, LN_THREADS, 0, st>>>(p); break;
+            case 4: ln_dx_kernel<4><<<grid, LN_THREADS, 0, st>>>(p); break;
+            default: ln_dx_kernel<8><<<grid, LN_THREADS, 0, st>>>(p); break;
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
