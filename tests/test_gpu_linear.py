@@ -91,6 +91,8 @@ def test_tiny_full(name):
     ("row", 256, 2048, 128, 8, 1),      # eight shards
     ("column", 512, 256, 1024, 4, 4),   # sequence-parallel token chunks
     ("row", 512, 1024, 256, 4, 4),
+    ("column", 1024, 512, 2048, 8, 8),  # eight shards and eight token chunks
+    ("row", 1024, 2048, 512, 8, 8),
 ])
 def test_ragged_full(split, T, din, dout, t, chunks):
     _run_full(custom_linear(T, din, dout, t, split, sigma_w=0.05, seq_chunks=chunks), seed=3)

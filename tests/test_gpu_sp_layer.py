@@ -82,6 +82,8 @@ def _run_full(w, p, seed=0):
     (333, 264, 1032, 3, 1, 0.2),    # ragged M, N and K tails
     (256, 2048, 2048, 8, 2, 0.5),   # eight shards, wide rows
     (128, 256, 1024, 2, 1, 0.0),    # no dropout: Out = X + MLP(LN(X))
+    (256, 6144, 1024, 2, 2, 0.1),   # LayerNorm rows of 3 vectors per thread (4-vector kernels)
+    (128, 16384, 512, 1, 1, 0.1),   # the widest rows the LayerNorm kernels take (h = 16384)
 ])
 def test_sp_layer_full(T, h, f, t, chunks, p):
     # weights with the workloads' standard deviation (0.02)
