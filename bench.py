@@ -719,13 +719,15 @@ def run_ours(args, torch):
 
     # End to end through the C ABI with host buffers.  Every step uploads its
     # inputs (the block: X and dZ; a linear layer: X and dY) from pinned host
-    # memory and downloads its forward and backward results.  The copies run
-    # on a second stream with double-buffered device activations, so the
-    # upload of step i+1 and the downloads of step i overlap step i's GEMMs, as
-    # a training loop that prefetches its next batch would.
+    # memory and downloads its forward and backward results.  Uploads and
+    # downloads run on two more streams with double-buffered device
+    # activations, so the upload of step i+1 overlaps step i's kernels and the
+    # downloads of step i overlap step i+1's, as a training loop that
+    # prefetches its next batch would.
     e2e = None
     if not args.no_e2e:
-        copy_stream = torch.cuda.Stream(dev)
+        up_stream = torch.cuda.Stream(dev)
+        down_stream = torch.cuda.Stream(dev)
         names = run.ins + run.outs
         host_in = {k: [x.cpu().pin_memory() for x in run.buffers(k)] for k in run.ins}
         host_out = {k: [torch.empty_like(x, device="cpu").pin_memory() for x in run.buffers(k)]
@@ -741,26 +743,26 @@ def run_ours(args, torch):
             for i in range(n):
                 b = i & 1
                 B = bufs[b]
-                with torch.cuda.stream(copy_stream):
+                with torch.cuda.stream(up_stream):
                     if i >= 2:  # step i-2 is done with this buffer set
-                        copy_stream.wait_event(ev["out_done"][b])
+                        up_stream.wait_event(ev["out_done"][b])
                     for k in run.ins:
                         for d, h in zip(B[k], host_in[k]):
                             d.copy_(h, non_blocking=True)
-                    ev["in_ready"][b].record(copy_stream)
+                    ev["in_ready"][b].record(up_stream)
                 stream.wait_event(ev["in_ready"][b])
                 run.forward(B, stream)
                 ev["fwd_done"][b].record(stream)
                 run.backward(B, stream)
                 ev["bwd_done"][b].record(stream)
-                with torch.cuda.stream(copy_stream):
-                    copy_stream.wait_event(ev["fwd_done"][b])
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(ev["fwd_done"][b])
                     for h, d in zip(host_out[fwd_out], B[fwd_out]):
                         h.copy_(d, non_blocking=True)
-                    copy_stream.wait_event(ev["bwd_done"][b])
+                    down_stream.wait_event(ev["bwd_done"][b])
                     for h, d in zip(host_out[bwd_out], B[bwd_out]):
                         h.copy_(d, non_blocking=True)
-                    ev["out_done"][b].record(copy_stream)
+                    ev["out_done"][b].record(down_stream)
 
         e2e_steps(2)
         torch.cuda.synchronize(dev)
@@ -768,9 +770,11 @@ def run_ours(args, torch):
         e2 = torch.cuda.Event(enable_timing=True)
         e3 = torch.cuda.Event(enable_timing=True)
         e2.record(stream)
-        copy_stream.wait_event(e2)  # the first upload starts inside the timed region
+        up_stream.wait_event(e2)  # the first upload starts inside the timed region
+        down_stream.wait_event(e2)
         e2e_steps(args.e2e_steps)
-        stream.wait_stream(copy_stream)  # ... and the last download ends inside it
+        stream.wait_stream(up_stream)
+        stream.wait_stream(down_stream)  # ... and the last download ends inside it
         e3.record(stream)
         barrier(dist, torch)
         st = binding.tpmlp_sync_check(stream)
@@ -788,7 +792,7 @@ def run_ours(args, torch):
                                          for k in run.outs for x in host_out[k]),
                "tokens_per_s": T * args.e2e_steps * world / (ms_e2e / 1e3),
                "steps": args.e2e_steps,
-               "overlap": "copies on a second stream, double-buffered activations"}
+               "overlap": "uploads and downloads on two more streams, double-buffered activations"}
 
     if rank == 0:
         cpu = None
