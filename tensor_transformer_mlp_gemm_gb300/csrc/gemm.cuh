@@ -454,12 +454,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish_pair();
     }
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < p.a_nmaps; ++i) ptx::prefetch_tensormap(&p.a_map[i]);
+        for (int i = 0; i < p.b_nmaps; ++i) ptx::prefetch_tensormap(&p.b_map[i]);
+    }
     // both CTAs' barriers and tensor memory exist before anything crosses
     ptx::tc_fence_before();
     __syncwarp();
     ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: the set-up above overlaps that kernel's last wave; nothing
+    // below touches global memory before it has completed.  The next kernel
+    // may be scheduled now (this grid is resident all at once, so its CTAs
+    // can only take SMs that this grid has left).
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     const int kblocks = (p.K + BK - 1) / BK;
     const int nk = kblocks * p.ksegs;
@@ -861,8 +872,17 @@ cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
         cudaError_t e = cudaMemsetAsync(p.counters, 0, sizeof(int) * 2 * left, stream);
         if (e != cudaSuccess) return e;
     }
-    kern<<<2 * clusters, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 #define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)               \
