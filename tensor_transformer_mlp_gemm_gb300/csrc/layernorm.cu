@@ -315,8 +315,7 @@ cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_
     return cudaGetLastError();
 }
 
-cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, int /*sm_count*/,
-                                    cudaStream_t st) {
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
     const int vecs = (p.h + 7) / 8;
     const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((vecs + LN_THREADS - 1) / LN_THREADS));

@@ -26,7 +26,7 @@ constexpr int LN_MAX_CHUNKS = 8;
 
 struct LnChunks {
     const void* in[LN_MAX_CHUNKS];
-    int n;
+    int n;           // chunks (the kernels find a row's chunk as row / rows)
     long long rows;  // rows per chunk
 };
 
@@ -79,8 +79,7 @@ inline int ln_param_splits(long long T, long long h, int sm_count) {
 }
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st);
-cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, int sm_count,
-                                    cudaStream_t st);
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, cudaStream_t st);
 // Three launches: dX per token row, the dgamma / dbeta partial column sums
 // over `splits` row splits, and their fixed-order finish.
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,

@@ -200,7 +200,7 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_
     db.h = s.h;
     db.drop = dropout_of(*sp);
     TPMLP_CUDA(timed(TPMLP_KERNEL_DROPOUT_BWD, 1, st,
-                     [&] { return launch_dropout_backward(db, s.T, dev->sm_count, st); }));
+                     [&] { return launch_dropout_backward(db, s.T, st); }));
 
     TPMLP_TRY(run_backward(s, dev, dz, xn, A_shards, B_shards, dxn, dA_shards, db1, dB_shards,
                            db2, regions_of(ws, L.blk), false, st));
