@@ -71,6 +71,9 @@ def parse_args():
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph (the per-kernel "
                          "times then come from eager steps run after the timed region)")
+    ap.add_argument("--cublas", action="store_true",
+                    help="also time torch.matmul (cuBLAS) on the block's six GEMM shapes, unsharded "
+                         "(an informative comparison, bf16 in and out, no fused epilogues)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -252,6 +255,49 @@ def gpu_selector(torch, dev_index):
     if vis:
         return vis.split(",")[dev_index]
     return str(dev_index)
+
+
+def cublas_reference(w, torch, dev, iters=20):
+    """torch.matmul (cuBLAS) on the MLP block's six GEMM shapes, unsharded, bf16
+    in and out: Y = X.A, Z = H.B, dH = dZ.B^T, dX = dY.A^T, dB = H^T.dZ,
+    dA = X^T.dY.  TFLOP/s per shape from CUDA events, after warm-up."""
+    T, h, f = w.tokens, w.hidden, w.ffn
+    bf = torch.bfloat16
+    X = torch.randn(T, h, device=dev, dtype=bf)
+    A = torch.randn(h, f, device=dev, dtype=bf)
+    B = torch.randn(f, h, device=dev, dtype=bf)
+    Hm = torch.randn(T, f, device=dev, dtype=bf)
+    dZ = torch.randn(T, h, device=dev, dtype=bf)
+    shapes = {"column_fwd (X.A)": (X, A), "row_fwd (H.B)": (Hm, B), "dgrad_h (dZ.B^T)": (dZ, B.t()),
+              "dgrad_x (dY.A^T)": (Hm, A.t()), "wgrad_b (H^T.dZ)": (Hm.t(), dZ),
+              "wgrad_a (X^T.dY)": (X.t(), Hm)}
+    out = {}
+    flop = 2.0 * T * h * f
+    for name, (a, b) in shapes.items():
+        for _ in range(3):
+            torch.matmul(a, b)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        out[name] = flop / (e0.elapsed_time(e1) / iters / 1e3) / 1e12
+    del X, A, B, Hm, dZ
+    torch.cuda.empty_cache()
+    return {"tflops": out, "note": "torch.matmul, unsharded shapes, bf16 out, no fused epilogues"}
+
+
+def theoretical_peak_tflops(torch, dev):
+    """SMs x 8192 dense bf16 FLOP/clk x maximum SM clock."""
+    try:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True, timeout=20)
+        mhz = float(out.stdout.strip().splitlines()[0])
+        return {"tflops": sms * 8192 * mhz * 1e6 / 1e12, "sms": sms, "max_sm_mhz": mhz}
+    except Exception:
+        return None
 
 
 # ---- CPU oracle ----------------------------------------------------------------------------
@@ -798,6 +844,10 @@ def run_ours(args, torch):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(w, run.inputs, args.cpu_seconds, args.sp_layer)
+        cublas = None
+        if args.cublas and hasattr(w, "hidden"):
+            cublas = cublas_reference(w, torch, dev)
+        theo = theoretical_peak_tflops(torch, dev)
         line = {"metric": run.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -806,8 +856,11 @@ def run_ours(args, torch):
                 "tokens_per_s": tokens_s,
                 "pct_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
                                      "sustained": value / world / peaks["bf16_tflops_sustained"],
-                                     "source": peak_src},
+                                     "source": peak_src,
+                                     "theoretical": (value / world / theo["tflops"]) if theo else None,
+                                     "theoretical_peak": theo},
                 "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "cublas_reference": cublas,
                 "clocks": clocks, "gpu_launches": int(sum(kcount.values())),
                 "cuda_graph": bool(args.graph),
                 "kernel_timing": ("CUDA events around each launch inside the timed region"
