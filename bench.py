@@ -257,10 +257,14 @@ def gpu_selector(torch, dev_index):
     return str(dev_index)
 
 
-def cublas_reference(w, torch, dev, iters=20):
+def cublas_reference(w, torch, dev, steps=300, warmup=10):
     """torch.matmul (cuBLAS) on the MLP block's six GEMM shapes, unsharded, bf16
-    in and out: Y = X.A, Z = H.B, dH = dZ.B^T, dX = dY.A^T, dB = H^T.dZ,
-    dA = X^T.dY.  TFLOP/s per shape from CUDA events, after warm-up."""
+    in and out (fp32 out for the weight gradients where torch.mm takes
+    out_dtype): Y = X.A, Z = H.B, dH = dZ.B^T, dX = dY.A^T, dB = H^T.dZ,
+    dA = X^T.dY, run back to back as one step and repeated for as many steps
+    as the timed region, so that cuBLAS sees the same power-capped clocks as
+    the library's step.  CUDA events around each GEMM; clocks sampled during
+    the loop."""
     T, h, f = w.tokens, w.hidden, w.ffn
     bf = torch.bfloat16
     X = torch.randn(T, h, device=dev, dtype=bf)
@@ -271,21 +275,53 @@ def cublas_reference(w, torch, dev, iters=20):
     shapes = {"column_fwd (X.A)": (X, A), "row_fwd (H.B)": (Hm, B), "dgrad_h (dZ.B^T)": (dZ, B.t()),
               "dgrad_x (dY.A^T)": (Hm, A.t()), "wgrad_b (H^T.dZ)": (Hm.t(), dZ),
               "wgrad_a (X^T.dY)": (X.t(), Hm)}
-    out = {}
+    outs = {k: torch.empty(a.shape[0], b.shape[1], device=dev, dtype=bf) for k, (a, b) in shapes.items()}
     flop = 2.0 * T * h * f
-    for name, (a, b) in shapes.items():
-        for _ in range(3):
-            torch.matmul(a, b)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            torch.matmul(a, b)
-        e1.record()
-        torch.cuda.synchronize(dev)
-        out[name] = flop / (e0.elapsed_time(e1) / iters / 1e3) / 1e12
-    del X, A, B, Hm, dZ
+    names = list(shapes)
+    # The weight gradients leave as fp32, like the library's; torch.mm's out_dtype
+    # form keeps cuBLAS's fp32 accumulator instead of rounding it to bf16.
+    wgrad_fp32 = True
+    try:
+        a, b = shapes["wgrad_b (H^T.dZ)"]
+        torch.mm(a[:128, :128], b[:128, :128], out_dtype=torch.float32)
+    except Exception:
+        wgrad_fp32 = False
+
+    def gemm(k):
+        a, b = shapes[k]
+        if wgrad_fp32 and k.startswith("wgrad"):
+            return torch.mm(a, b, out_dtype=torch.float32)
+        return torch.matmul(a, b, out=outs[k])
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in names] for _ in range(steps)]
+    for _ in range(warmup):
+        for k in names:
+            gemm(k)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_selector(torch, dev.index or 0))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        for n, k in enumerate(names):
+            ev[s][n][0].record()
+            gemm(k)
+            ev[s][n][1].record()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    per = {}
+    for n, k in enumerate(names):
+        ms = sum(ev[s][n][0].elapsed_time(ev[s][n][1]) for s in range(steps)) / steps
+        per[k] = flop / (ms / 1e3) / 1e12
+    ms_step = e0.elapsed_time(e1) / steps
+    del X, A, B, Hm, dZ, outs
     torch.cuda.empty_cache()
-    return {"tflops": out, "note": "torch.matmul, unsharded shapes, bf16 out, no fused epilogues"}
+    return {"tflops": per, "step_tflops": 6 * flop / (ms_step / 1e3) / 1e12, "ms_per_step": ms_step,
+            "steps": steps, "clocks": clocks, "wgrad_out": "fp32" if wgrad_fp32 else "bf16",
+            "note": "torch.matmul / torch.mm, unsharded shapes, bf16 out (weight gradients as "
+                    "wgrad_out), no fused epilogues, six GEMMs back to back per step"}
 
 
 def theoretical_peak_tflops(torch, dev):
@@ -846,7 +882,7 @@ def run_ours(args, torch):
             cpu = cpu_baseline(w, run.inputs, args.cpu_seconds, args.sp_layer)
         cublas = None
         if args.cublas and hasattr(w, "hidden"):
-            cublas = cublas_reference(w, torch, dev)
+            cublas = cublas_reference(w, torch, dev, steps=args.steps)
         theo = theoretical_peak_tflops(torch, dev)
         line = {"metric": run.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

@@ -84,6 +84,13 @@ __device__ __forceinline__ float gelu_grad_f(float y) {
 
 // ---- bounded waits -------------------------------------------------------------
 
+// Sleeps in short naps until this SM's clock reaches `deadline` (returns at once
+// if it already has).  The deadline is at most a few thousand clocks ahead; the
+// nap count is capped all the same.
+__device__ __forceinline__ void pace_until(long long deadline) {
+    for (int i = 0; i < 4096 && clock64() < deadline; ++i) __nanosleep(32);
+}
+
 // Waits for phase `parity` of `bar`.  Gives up (returns false) when another
 // role has aborted, or when timeout_ns has elapsed (then this role aborts the
 // CTA and records `code` in the device error word).
@@ -671,10 +678,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         };
 
         // fp32 outputs (the weight gradients: short K, 128 KB per CTA per tile)
-        // are stored paced over about half the time the next tile's MMAs take
-        // (measured as the gap between accumulator hand-overs): stored in one
-        // burst, all pairs' stores would meet the next tiles' first loads
-        uint64_t t_prev_full = 0;
+        // are stored paced over about half the time the next tile's MMAs take:
+        // stored in one burst, all pairs' stores would meet the next tiles' first
+        // loads.  The schedule is a deadline per chunk in SM clocks, derived from
+        // the tile's K steps, not from the measured time between tiles: a paced
+        // epilogue that falls behind (slow stores) does not wait, so the pacing
+        // cannot feed back into a longer tile period.
         int lt = 0;
         WorkItem it;
         for (int j = 0; work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
@@ -704,15 +713,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             if (*epi_fail) break;
             __syncwarp();
             ptx::tc_fence_after();
-            unsigned pace_ns = 0;
+            long long pace_t0 = 0, pace_clk = 0;
             if constexpr (EPI == EPI_F32) {
-                const uint64_t t_now = ptx::globaltimer_ns();
-                if (t_prev_full != 0 && it.unit < 0) {
-                    const uint64_t gap = t_now - t_prev_full;  // ~ one tile of MMAs
-                    const uint64_t ns = gap * 9 / 128;         // x 7 chunks ~ half of it
-                    pace_ns = static_cast<unsigned>(ns < 4000 ? ns : 4000);
+                if (it.unit < 0) {
+                    pace_clk = static_cast<long long>(it.kend - it.kbeg) * PACE_CLK_PER_KBLOCK;
+                    pace_t0 = clock64();
                 }
-                t_prev_full = t_now;
             }
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
@@ -738,7 +744,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
                     epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, cur);
-                    if (pace_ns && c > 0) __nanosleep(pace_ns);
+                    if (pace_clk && c > 0) pace_until(pace_t0 + c * pace_clk);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                 }
                 ptx::tc_fence_before();

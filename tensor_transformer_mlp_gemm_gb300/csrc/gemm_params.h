@@ -30,6 +30,13 @@ constexpr int EPI_WARPS = 4;
 constexpr int EPI_CHUNK = 32;                 // accumulator columns per epilogue step
 constexpr int EPI_BUF_BYTES = 4096;           // one staged 32 x 32 chunk (fp32, or 2 x bf16)
 constexpr int EPI_STAGE_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;  // double-buffered per warp
+// fp32 output pacing: one BK step of a pair's 256 x 256 MMAs takes 4 x 128 SM
+// clocks; chunk c of a tile is stored no earlier than c x PACE_CLK_PER_KBLOCK x
+// (the tile's K steps) clocks after its accumulator arrived, which spreads the
+// eight chunk stores over about two thirds of the next tile's MMA time (7 x 48
+// of 512 clocks per K step; measured best among 20..96 on the weight gradients
+// of the 175B-class layer).
+constexpr int PACE_CLK_PER_KBLOCK = 48;
 constexpr int GEMM_SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGE_BYTES + BAR_BYTES;
 constexpr int MAX_MAPS = 8;
 // Tail split: when the tiles do not fill the last wave of pairs, the leftover
