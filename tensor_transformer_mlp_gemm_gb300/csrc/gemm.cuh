@@ -678,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         };
 
         // fp32 outputs (the weight gradients: short K, 128 KB per CTA per tile)
-        // are stored paced over about half the time the next tile's MMAs take:
+        // are stored paced over most of the time the next tile's MMAs take:
         // stored in one burst, all pairs' stores would meet the next tiles' first
         // loads.  The schedule is a deadline per chunk in SM clocks, derived from
         // the tile's K steps, not from the measured time between tiles: a paced
