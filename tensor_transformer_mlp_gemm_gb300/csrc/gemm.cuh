@@ -715,7 +715,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             ptx::tc_fence_after();
             long long pace_t0 = 0, pace_clk = 0;
             if constexpr (EPI == EPI_F32) {
-                if (it.unit < 0) {
+                // only while this pair has a next tile whose main loop the stores can
+                // hide under; the last tile's stores go out at once
+                WorkItem nx;
+                if (it.unit < 0 && work_item(p, cluster, nclusters, j + 1, nk, nx)) {
                     pace_clk = static_cast<long long>(it.kend - it.kbeg) * PACE_CLK_PER_KBLOCK;
                     pace_t0 = clock64();
                 }
