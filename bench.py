@@ -21,6 +21,11 @@ Out = X + Dropout(MLP(LN(X))) (LayerNorm and dropout per token chunk); the
 FLOP count stays the block's 12*T*h*f (the LayerNorm and dropout passes are
 timed but counted as no FLOP).
 
+--cublas adds an informative comparison: torch.matmul / torch.mm (cuBLAS) on
+the block's six GEMM shapes, unsharded, back to back as one step for as many
+steps as the timed region (weight gradients with fp32 output where torch.mm
+takes out_dtype), with its own clock record ("cublas_reference").
+
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded token sample of the same layer per step (same metric and unit).
 Under torchrun with N > 1 every rank runs an independent replica of the
