@@ -24,7 +24,9 @@ timed but counted as no FLOP).
 --cublas adds an informative comparison: torch.matmul / torch.mm (cuBLAS) on
 the block's six GEMM shapes, unsharded, back to back as one step for as many
 steps as the timed region (weight gradients with fp32 output where torch.mm
-takes out_dtype), with its own clock record ("cublas_reference").
+takes out_dtype), with its own clock record ("cublas_reference"), and the
+whole block composed from PyTorch ops (cuBLAS GEMMs, PyTorch's GeLU and its
+backward, column sums; "cublas_reference.torch_block").
 
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded token sample of the same layer per step (same metric and unit).
@@ -77,8 +79,8 @@ def parse_args():
                     help="time replays of one step captured in a CUDA graph (the per-kernel "
                          "times then come from eager steps run after the timed region)")
     ap.add_argument("--cublas", action="store_true",
-                    help="also time torch.matmul (cuBLAS) on the block's six GEMM shapes, unsharded "
-                         "(an informative comparison, bf16 in and out, no fused epilogues)")
+                    help="also time cuBLAS on the block's six GEMM shapes (unsharded, back to back) "
+                         "and the whole block composed from PyTorch ops (informative comparisons)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -327,6 +329,58 @@ def cublas_reference(w, torch, dev, steps=300, warmup=10):
             "steps": steps, "clocks": clocks, "wgrad_out": "fp32" if wgrad_fp32 else "bf16",
             "note": "torch.matmul / torch.mm, unsharded shapes, bf16 out (weight gradients as "
                     "wgrad_out), no fused epilogues, six GEMMs back to back per step"}
+
+
+def torch_block_reference(w, inputs, torch, dev, steps=300, warmup=10):
+    """The same block composed from PyTorch CUDA ops, unsharded: cuBLAS GEMMs
+    (the biases in their epilogue through addmm), PyTorch's tanh-GeLU and its
+    backward, fp32 column sums.  Forward Y = X.A + b1, H = GeLU(Y), Z = H.B + b2;
+    backward dH = dZ.B^T, dY = GeLU'(Y) * dH, dX = dY.A^T, dB = H^T.dZ and
+    dA = X^T.dY (fp32 where torch.mm takes out_dtype), db1, db2.  Same seeded
+    inputs, timed over as many steps as the timed region, clocks sampled."""
+    import torch.nn.functional as F
+    X, A, b1, B, b2, dZ = (inputs[k].to(dev) for k in ("X", "A", "b1", "B", "b2", "dZ"))
+    try:
+        torch.mm(X[:128, :128], A[:128, :128], out_dtype=torch.float32)
+        fp32 = True
+    except Exception:
+        fp32 = False
+
+    def wgrad(a, b):
+        return torch.mm(a, b, out_dtype=torch.float32) if fp32 else torch.mm(a, b)
+
+    def step():
+        Y = torch.addmm(b1, X, A)
+        H = F.gelu(Y, approximate="tanh")
+        Z = torch.addmm(b2, H, B)
+        dH = torch.mm(dZ, B.t())
+        dY = torch.ops.aten.gelu_backward(dH, Y, approximate="tanh")
+        dX = torch.mm(dY, A.t())
+        dB = wgrad(H.t(), dZ)
+        dA = wgrad(X.t(), dY)
+        db1 = dY.sum(0, dtype=torch.float32)
+        db2 = dZ.sum(0, dtype=torch.float32)
+        return Z, dX, dA, dB, db1, db2
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_selector(torch, dev.index or 0))
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / steps
+    del X, A, b1, B, b2, dZ
+    torch.cuda.empty_cache()
+    return {"value": w.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "steps": steps, "clocks": clocks, "wgrad_out": "fp32" if fp32 else "bf16",
+            "note": "the block from PyTorch ops (addmm, gelu tanh, gelu_backward, mm, sum), "
+                    "unsharded, same inputs"}
 
 
 def theoretical_peak_tflops(torch, dev):
@@ -888,6 +942,9 @@ def run_ours(args, torch):
         cublas = None
         if args.cublas and hasattr(w, "hidden"):
             cublas = cublas_reference(w, torch, dev, steps=args.steps)
+            if not args.sp_layer:
+                cublas["torch_block"] = torch_block_reference(w, run.inputs, torch, dev,
+                                                              steps=args.steps)
         theo = theoretical_peak_tflops(torch, dev)
         line = {"metric": run.metric, "value": value, "unit": "TFLOP/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
