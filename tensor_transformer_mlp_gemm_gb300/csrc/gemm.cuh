@@ -28,11 +28,6 @@
 // shared memory and each SM keeps 192 KB of operands in flight while needing
 // only 64 B per clock at full MMA rate (a single-CTA 128 x 256 tile needs 96).
 // The pair's accumulator rows live in each CTA's own tensor memory.
-// Optionally (GemmParams::b_multicast) two pairs form a cluster of four CTAs
-// on vertically adjacent tiles with the same B tile: each K step one of them
-// fetches every B box and multicasts it to the same CTA of both pairs, which
-// halves the B traffic from L2; a stage is then free once both pairs' MMAs
-// have released it.
 //
 // CTA layout (192 threads, persistent over tiles; both CTAs of the pair):
 //   warp 0      TMA producer (one elected thread): this CTA's A and B halves
