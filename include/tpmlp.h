@@ -332,21 +332,6 @@ tpmlp_status tpmlp_set_split_min_kblocks(int kblocks);
  * it.  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_head_prefetch(int kblocks);
 
-/* B multicast of the GEMMs: with `enable` = 1, a GEMM that has at least two
- * 256-row tiles in M and whose clusters of two CTA pairs leave at most 5 % of
- * their last wave idle runs as such clusters: the two pairs take vertically
- * adjacent tiles with the same B tile, and on every K step one of them
- * fetches each 128-row B box and multicasts it (TMA) to the same CTA of both
- * pairs, which halves the L2-to-SM traffic of B.  Such a GEMM never splits a
- * tile along K.  With `enable` = 2 every GEMM with at least two tiles in M
- * runs as clusters of two pairs (for tests).  0 (default) runs every GEMM as
- * single pairs.  0, 1 or 2, else TPMLP_ERR_INVALID_ARG.  Results stay
- * deterministic and equal the single-pair ones bitwise, except in tiles the
- * single-pair launch splits along K (tpmlp_set_split_min_kblocks), which sum
- * the same products in another order.  Affects launches enqueued after the
- * call. */
-tpmlp_status tpmlp_set_b_multicast(int enable);
-
 /* Upper bound, in nanoseconds, on any single wait inside a kernel of this
  * library (default 2e9).  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);

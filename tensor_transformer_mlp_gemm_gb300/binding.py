@@ -40,7 +40,6 @@ EXPORTED = (
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
     "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
     "tpmlp_set_head_prefetch",
-    "tpmlp_set_b_multicast",
 )
 
 
@@ -97,8 +96,6 @@ _lib.tpmlp_set_split_min_kblocks.restype = ctypes.c_int
 _lib.tpmlp_set_split_min_kblocks.argtypes = [ctypes.c_int]
 _lib.tpmlp_set_head_prefetch.restype = ctypes.c_int
 _lib.tpmlp_set_head_prefetch.argtypes = [ctypes.c_int]
-_lib.tpmlp_set_b_multicast.restype = ctypes.c_int
-_lib.tpmlp_set_b_multicast.argtypes = [ctypes.c_int]
 _lib.tpmlp_set_wait_timeout_ns.restype = ctypes.c_int
 _lib.tpmlp_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.tpmlp_selftest_stalled_gemm.restype = ctypes.c_int
@@ -245,12 +242,6 @@ def tpmlp_set_split_min_kblocks(kblocks: int) -> None:
 
 def tpmlp_set_head_prefetch(kblocks: int) -> None:
     _check(_lib.tpmlp_set_head_prefetch(int(kblocks)), "tpmlp_set_head_prefetch")
-
-
-def tpmlp_set_b_multicast(mode: int) -> None:
-    """0 off, 1 on where the clusters fill their waves, 2 on wherever M has
-    two or more tiles."""
-    _check(_lib.tpmlp_set_b_multicast(int(mode)), "tpmlp_set_b_multicast")
 
 
 def tpmlp_set_wait_timeout_ns(ns: int) -> None:

@@ -144,27 +144,19 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const 
 // runs fastest, so the CTAs that run at the same time share their B tiles
 // (and, across the band, their A panels) through L2.  (group, n-tile) pairs
 // form one combined N axis.
-// With CM pairs per cluster a tile index names a cluster tile: CM vertically
-// adjacent pair tiles with the same group and n-tile (the same B tile); pair
-// `pair` of the cluster takes M-tile CM * mt + pair.  A pair whose M-tile lies
-// past the last one (odd M-tile count) computes on zero-filled rows and stores
-// nothing.
-template <int CM>
-__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int pair, int& g,
-                                            int& m0, int& n0) {
-    const int mtiles = (p.mtiles + CM - 1) / CM;
-    const int band = CM == 1 ? p.band : max(1, p.band / CM);
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& g, int& m0,
+                                            int& n0) {
     const int nt_total = p.ntiles * p.groups;
-    const int band_tiles = band * nt_total;
+    const int band_tiles = p.band * nt_total;
     const int b = tile / band_tiles;
     const int r = tile - b * band_tiles;
-    const int mt_first = b * band;
-    const int rows_here = min(band, mtiles - mt_first);
+    const int mt_first = b * p.band;
+    const int rows_here = min(p.band, p.mtiles - mt_first);
     const int mt = mt_first + r % rows_here;
     const int ntg = r / rows_here;
     g = ntg / p.ntiles;
     n0 = (ntg - g * p.ntiles) * BN;
-    m0 = (mt * CM + pair) * CLUSTER_M;
+    m0 = mt * CLUSTER_M;
 }
 
 // ---- work items -------------------------------------------------------------------
@@ -249,27 +241,6 @@ __device__ __forceinline__ void load_operand(const OperandCursor& c, int kc, uin
 #pragma unroll
             for (int j = 0; j < ROWS / MN_CHUNK; ++j)
                 ptx::tma_load_2d_pair(dst + j * MN_CHUNK_BYTES, c.map, c.r + j * MN_CHUNK, k, bar);
-        }
-    }
-}
-
-// The same boxes as load_operand, multicast: each box lands at offset `dst` of
-// every CTA in `mask` and completes on the barrier at the offset of `bar` in
-// the even CTA of each receiving CTA's pair.
-template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand_mc(const OperandCursor& c, int kc, uint32_t dst,
-                                                uint32_t bar, uint16_t mask) {
-    const int k = c.kbase + kc;
-    if constexpr (!MN) {
-        ptx::tma_load_2d_pair_multicast(dst, c.map, k, c.r, bar, mask);
-    } else {
-        if (c.mn3d) {
-            ptx::tma_load_3d_pair_multicast(dst, c.map, 0, k, c.r / MN_CHUNK, bar, mask);
-        } else {
-#pragma unroll
-            for (int j = 0; j < ROWS / MN_CHUNK; ++j)
-                ptx::tma_load_2d_pair_multicast(dst + j * MN_CHUNK_BYTES, c.map,
-                                                c.r + j * MN_CHUNK, k, bar, mask);
         }
     }
 }
@@ -444,15 +415,9 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
 
 // ---- the kernel ---------------------------------------------------------------------
 
-// CM = CTA pairs per cluster: 1, or 2 for clusters of two pairs that share
-// every B box (each K step one pair fetches it and multicasts it to the same
-// CTA of both pairs, so the L2-to-SM traffic of B halves).  Every stage's
-// bytes, A and B, complete on the even CTA of the receiving pair, as for a
-// single pair.
-template <bool A_MN, bool B_MN, int EPI, int CM>
-__global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     tpmlp_gemm_kernel(const __grid_constant__ GemmParams p) {
-    static_assert(CM == 1 || CM == 2, "one or two CTA pairs per cluster");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -472,19 +437,14 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int crank = static_cast<int>(ptx::cluster_ctarank());
-    const int rank = crank & 1;   // CTA within its pair
-    const int pair = crank >> 1;  // pair within the cluster
-    const int lead = crank & ~1;  // cluster rank of this pair's even CTA
-    const int cluster = blockIdx.x / (2 * CM);
-    const int nclusters = gridDim.x / (2 * CM);
+    const int rank = static_cast<int>(ptx::cluster_ctarank());  // CTA within its pair
+    const int cluster = blockIdx.x / 2;
+    const int nclusters = gridDim.x / 2;
 
     if (threadIdx.x == 0) {
-        // with two pairs every "empty" barrier counts one release from each
-        // pair's MMAs (each producer writes into both pairs)
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
-            ptx::mbar_init(bar_empty + 8 * s, CM);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar_tfull + 8 * a, 1);
@@ -523,7 +483,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer (both CTAs) ----------------
-            const uint32_t even_full = ptx::mapa_shared(bar_full, lead);
+            const uint32_t even_full = ptx::mapa_shared(bar_full, 0);
             int stage = 0;
             uint32_t phase = 0;
             long long fills = 0;
@@ -541,7 +501,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
                         ptx::griddep_launch_dependents();
                 }
                 int g, m0, n0;
-                decode_tile<CM>(p, it.tile, pair, g, m0, n0);
+                decode_tile(p, it.tile, g, m0, n0);
                 const int a_row = m0 + rank * BM;
                 const int b_row = n0 + rank * B_ROWS;
                 // segment and K step advance by increments; the map and row of each
@@ -559,7 +519,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
                     WorkItem nx;
                     if (work_item(p, cluster, nclusters, j + 1, nk, nx)) {
                         int ng, nm0, nn0;
-                        decode_tile<CM>(p, nx.tile, pair, ng, nm0, nn0);
+                        decode_tile(p, nx.tile, ng, nm0, nn0);
                         const int nseg = nx.kbeg / kblocks;
                         const int nkb = nx.kbeg - nseg * kblocks;
                         const OperandCursor pa =
@@ -596,15 +556,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
                             if (rank == 0)  // counts both CTAs' bytes
                                 ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * STAGE_BYTES);
                             load_operand<A_MN, BM>(ca, kb * BK, sa, full);
-                            if constexpr (CM == 1) {
-                                load_operand<B_MN, B_ROWS>(cb, kb * BK, sa + A_STAGE_BYTES, full);
-                            } else if ((kk & 1) == pair) {
-                                // the pair whose turn it is (K step parity) fetches
-                                // this CTA's B box for the same CTA of both pairs
-                                load_operand_mc<B_MN, B_ROWS>(
-                                    cb, kb * BK, sa + A_STAGE_BYTES, full,
-                                    static_cast<uint16_t>((1u << rank) | (1u << (rank + 2))));
-                            }
+                            load_operand<B_MN, B_ROWS>(cb, kb * BK, sa + A_STAGE_BYTES, full);
                             ++fills;
                         }
                         if (++stage == STAGES) {
@@ -670,18 +622,15 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
                                            operand_desc<B_MN>(sb, k), IDESC,
                                            (kk > it.kbeg || k > 0) ? 1u : 0u);
                     }
-                    // the stage is free again in this pair's CTAs and, with two
-                    // pairs, in the other pair's (whose producers also fill it)
-                    ptx::mma_commit_pair_multicast(bar_empty + 8 * stage,
-                                                   CM == 1 ? 0x3 : 0xF);
+                    // the stage is free again in both CTAs of the pair
+                    ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (ok)
-                    ptx::mma_commit_pair_multicast(bar_tfull + 8 * acc,
-                                                   static_cast<uint16_t>(0x3u << lead));
+                    ptx::mma_commit_pair_multicast(bar_tfull + 8 * acc, 0x3);
             }
             // Every MMA this thread issued must finish before TMEM is freed.
             ptx::mma_commit_pair(bar_drain);
@@ -702,7 +651,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
         const int row = quarter * 32 + lane;
         uint8_t* stage_buf = epi_area + (warp - 2) * (2 * EPI_BUF_BYTES);
         const uint32_t stage_u32 = epi0 + (warp - 2) * (2 * EPI_BUF_BYTES);
-        const uint32_t even_tempty = ptx::mapa_shared(bar_tempty, lead);
+        const uint32_t even_tempty = ptx::mapa_shared(bar_tempty, 0);
         int chunk_seq = 0;
 
         // Stage 32 values per lane as this warp's 32 x 32 box and store it
@@ -741,7 +690,7 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
         WorkItem it;
         for (int j = 0; work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
             int g, mp, n0;
-            decode_tile<CM>(p, it.tile, pair, g, mp, n0);
+            decode_tile(p, it.tile, g, mp, n0);
             const int m0 = mp + rank * BM;  // this CTA's first row
             const int acc = lt & 1;
             const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
@@ -889,23 +838,23 @@ __global__ void __cluster_dims__(2 * CM, 1, 1) __launch_bounds__(GEMM_THREADS, 1
     }
 }
 
-// Clusters of CM CTA pairs of this kernel variant that fit on the GPU at once
-// (queried once per variant).
-template <bool A_MN, bool B_MN, int EPI, int CM>
+// CTA pairs of this kernel variant that fit on the GPU at once (queried once
+// per variant).
+template <bool A_MN, bool B_MN, int EPI>
 cudaError_t max_active_clusters(int& out) {
     static int max_clusters = 0;
     if (max_clusters == 0) {
-        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI, CM>;
+        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              GEMM_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * CM, 1, 1);
+        cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2 * CM;
+        attr.val.clusterDim.x = 2;
         attr.val.clusterDim.y = 1;
         attr.val.clusterDim.z = 1;
         cfg.attrs = &attr;
@@ -921,10 +870,10 @@ cudaError_t max_active_clusters(int& out) {
 }
 
 // Launched as a programmatic dependent of the previous kernel in the stream.
-template <bool A_MN, bool B_MN, int EPI, int CM>
+template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_variant(const GemmParams& p, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * CM * clusters, 1, 1);
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
     cfg.stream = stream;
@@ -933,35 +882,17 @@ cudaError_t launch_variant(const GemmParams& p, int clusters, cudaStream_t strea
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tpmlp_gemm_kernel<A_MN, B_MN, EPI, CM>, p);
+    return cudaLaunchKernelEx(&cfg, tpmlp_gemm_kernel<A_MN, B_MN, EPI>, p);
 }
 
-// Persistent launch, capped at the clusters that fit on the GPU at once.
-// With B multicast on (GemmParams::b_multicast = 1) a GEMM of at least two
-// pair tiles in M whose cluster tiles fill all but at most 5 % of their last
-// wave runs as clusters of two pairs (= 2: every GEMM of at least two pair
-// tiles in M); every other GEMM as single pairs, where the tiles of an
-// incomplete last wave get their K range split across the pairs that would
-// otherwise idle.
+// Persistent launch, capped at the pairs that fit on the GPU at once; the
+// tiles of an incomplete last wave get their K range split across the pairs
+// that would otherwise idle.
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
     GemmParams p = p_in;
-    if (p.b_multicast && p.mtiles >= 2) {
-        int P2 = 0;
-        cudaError_t e = max_active_clusters<A_MN, B_MN, EPI, 2>(P2);
-        if (e != cudaSuccess) return e;
-        const int tiles_c = ((p.mtiles + 1) / 2) * p.ntiles * p.groups;
-        const long long waves = (tiles_c + P2 - 1) / P2;
-        if (p.b_multicast == 2 || (tiles_c >= P2 && (waves * P2 - tiles_c) * 20 <= waves * P2)) {
-            p.total_tiles = tiles_c;
-            p.dp_tiles = tiles_c;
-            p.units = 0;
-            p.splits = 1;
-            return launch_variant<A_MN, B_MN, EPI, 2>(p, tiles_c < P2 ? tiles_c : P2, stream);
-        }
-    }
     int P = 0;
-    cudaError_t e = max_active_clusters<A_MN, B_MN, EPI, 1>(P);
+    cudaError_t e = max_active_clusters<A_MN, B_MN, EPI>(P);
     if (e != cudaSuccess) return e;
     const int nk = ((p.K + BK - 1) / BK) * p.ksegs;
     const int full = p.total_tiles / P;
@@ -985,7 +916,7 @@ cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
         e = cudaMemsetAsync(p.counters, 0, sizeof(int) * 2 * left, stream);
         if (e != cudaSuccess) return e;
     }
-    return launch_variant<A_MN, B_MN, EPI, 1>(p, clusters, stream);
+    return launch_variant<A_MN, B_MN, EPI>(p, clusters, stream);
 }
 
 #define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)               \

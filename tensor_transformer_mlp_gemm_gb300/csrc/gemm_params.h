@@ -90,9 +90,6 @@ struct GemmParams {
     int split_min_kblocks;  // split only when a tile has at least this many K steps
     int head_prefetch;      // at a tile's start, prefetch this many K steps of the next
                             // tile's operands into L2 (0 = off)
-    int b_multicast;        // 1: GEMMs that fill their waves run as clusters of two
-                            // pairs sharing each B box by TMA multicast; 2: every
-                            // GEMM with at least two pair tiles in M does
     CUtensorMap part_map;   // fp32 [MAX_SPLIT_UNITS * CLUSTER_M, BN] partial tiles
     const float* partial;   // same buffer, for the summing loads
     int* counters;          // [MAX_SPLIT_UNITS][2] arrivals per leftover tile and CTA

@@ -161,55 +161,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t 
                  : "memory");
 }
 
-// 2-D tiled load multicast to every CTA in cta_mask: the box lands at offset
-// `dst` of each of those CTAs' shared memory and its bytes complete on the
-// mbarrier at offset `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      int32_t x, int32_t y, uint32_t bar,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
-// Pair forms of the multicast loads (tcgen05 CTA pairs): the box lands at
-// offset `dst` of every CTA in cta_mask, and its bytes complete on the mbarrier
-// at the offset of `bar` in the even CTA of each receiving CTA's pair (`bar`
-// is a shared::cluster address of an even CTA's barrier).
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           int32_t x, int32_t y, uint32_t bar,
-                                                           uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-        "bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair_multicast(uint32_t dst, const CUtensorMap* map,
-                                                           int32_t x, int32_t y, int32_t z,
-                                                           uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-        "bytes.multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
-// 3-D tiled load multicast to every CTA in cta_mask (same landing and
-// completion rule as tma_load_2d_multicast): coordinates {x, y, z}.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      int32_t x, int32_t y, int32_t z, uint32_t bar,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // 2-D tiled store shared -> global, tracked by the issuing thread's bulk
 // async-groups.  Elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
@@ -333,16 +284,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// Same as mma_commit, arriving on the mbarrier at offset `bar` in every CTA
-// of cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
         : "memory");
 }
 

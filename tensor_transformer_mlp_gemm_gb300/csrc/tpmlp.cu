@@ -54,7 +54,6 @@ DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = 2000000000ULL;
 int g_split_min_kblocks = DEFAULT_SPLIT_MIN_KBLOCKS;
 int g_head_prefetch = 0;
-int g_b_multicast = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -219,7 +218,6 @@ bool attach_split(GemmParams& p, void* split_part, void* split_cnt) {
     p.counters = reinterpret_cast<int*>(split_cnt);
     p.split_min_kblocks = g_split_min_kblocks;
     p.head_prefetch = g_head_prefetch;
-    p.b_multicast = g_b_multicast;
     return true;
 }
 
@@ -568,13 +566,6 @@ TPMLP_API tpmlp_status tpmlp_set_head_prefetch(int kblocks) {
     if (kblocks < 0 || kblocks > 64) return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     g_head_prefetch = kblocks;
-    return TPMLP_OK;
-}
-
-TPMLP_API tpmlp_status tpmlp_set_b_multicast(int enable) {
-    if (enable < 0 || enable > 2) return TPMLP_ERR_INVALID_ARG;
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_b_multicast = enable;
     return TPMLP_OK;
 }
 
