@@ -28,6 +28,12 @@ takes out_dtype), with its own clock record ("cublas_reference"), and the
 whole block composed from PyTorch ops (cuBLAS GEMMs, PyTorch's GeLU and its
 backward, column sums; "cublas_reference.torch_block").
 
+After the main timed loop a sustained sub-record ("sustained") times at least
+3 s of back-to-back steps with its own clock record, long enough for the
+GPU's power cap to set the clock.  The roofline fraction of the main line is
+taken against the burst bf16 peak when its timed region lasted under 2 s and
+against the sustained peak otherwise; both fractions ride along.
+
 --impl reference times the fp64 CPU oracle on the host cores instead, on a
 bounded token sample of the same layer per step (same metric and unit).
 Under torchrun with N > 1 every rank runs an independent replica of the
@@ -52,6 +58,12 @@ SP_EPS, SP_P, SP_SEED = 1e-5, 0.1, 1234
 LINEAR_METRIC = ("TP linear layer (attention projection) fwd+bwd TFLOP/s and tokens/s on 1 GB300; "
                  "% of BF16 dense peak")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# A timed region shorter than BURST_MAX_S runs before the power cap pulls the
+# clock down, so its kernels are compared with the burst peak; a longer one
+# with the sustained peak.  The sustained sub-record times at least
+# SUSTAINED_MIN_S of back-to-back steps after the main loop.
+BURST_MAX_S = 2.0
+SUSTAINED_MIN_S = 3.0
 
 
 def parse_args():
@@ -85,6 +97,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sustained", action="store_true",
+                    help="skip the >= 3 s power-capped sub-record after the main loop")
     return ap.parse_args()
 
 
@@ -821,6 +835,9 @@ def run_ours(args, torch):
     tokens_s = T * args.steps * world / (ms / 1e3)
 
     peaks, peak_src = load_peaks()
+    # the peak that matches how long the timed region ran
+    timed_s = ms / 1e3
+    peak_key = "bf16_tflops_sustained" if timed_s >= BURST_MAX_S else "bf16_tflops"
     # dominant kernel: the kernel kind with the largest share of device time
     total_k = sum(kms.values())
     kernels = {}
@@ -832,17 +849,20 @@ def run_ours(args, torch):
     if dom in run.gemm_kinds:
         achieved = run.gemm_flops / (kernels[dom]["ms_per_launch"] / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "peak": peaks[peak_key], "unit": "TFLOP/s",
+                "frac": achieved / peaks[peak_key],
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "traffic": measured_traffic(dom, w.name),
-                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long "
-                               f"step); frac of burst {peaks['bf16_tflops']}: "
-                               f"{achieved / peaks['bf16_tflops']:.3f}",
+                "peak_source": f"{peak_src} {peak_key}: the timed region lasted {timed_s:.2f} s "
+                               f"({'at least' if timed_s >= BURST_MAX_S else 'under'} "
+                               f"{BURST_MAX_S:g} s)",
                 "flops_per_launch": run.gemm_flops}
     else:
         achieved = run.colsum_bytes / 1e9 / (kms[dom] / args.steps / 1e3)
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": f"{peak_src} hbm_gbs"}
     if "bias_grad" in kernels:
         cs_ms = kms["bias_grad"] / args.steps
         kernels["bias_grad"]["gb_per_s"] = run.colsum_bytes / (cs_ms / 1e3) / 1e9
@@ -857,6 +877,39 @@ def run_ours(args, torch):
         if name in kernels:
             kernels[name]["tflops"] = run.gemm_flops / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
     launches_per_step = sum(kcount.values()) / args.steps
+
+    # Sustained sub-record: at least SUSTAINED_MIN_S of back-to-back steps, long
+    # enough for the power cap to set the clock, with its own clock record.
+    sustained = None
+    if not args.no_sustained:
+        n_sus = max(args.steps, int(SUSTAINED_MIN_S * 1e3 / (ms / args.steps)) + 1)
+        sampler_s = ClockSampler(gpu_selector(torch, local))
+        sampler_s.start()
+        time.sleep(0.5)
+        e4 = torch.cuda.Event(enable_timing=True)
+        e5 = torch.cuda.Event(enable_timing=True)
+        barrier(dist, torch)
+        e4.record(stream)
+        for _ in range(n_sus):
+            if graph is None:
+                run.step(stream)
+            else:
+                graph.replay()
+        e5.record(stream)
+        barrier(dist, torch)
+        clocks_s = sampler_s.stop()
+        st = binding.tpmlp_sync_check(stream)
+        if st != binding.TPMLP_OK:
+            raise RuntimeError(f"sustained loop failed: {binding.tpmlp_status_string(st)}")
+        ms_s = max_over_ranks(dist, torch, e4.elapsed_time(e5))
+        v_s = flops_step * n_sus * world / (ms_s / 1e3) / 1e12
+        sustained = {"value": v_s, "unit": "TFLOP/s", "steps": n_sus, "seconds": ms_s / 1e3,
+                     "ms_per_step": ms_s / n_sus,
+                     "tokens_per_s": T * n_sus * world / (ms_s / 1e3),
+                     "frac_of_sustained_peak": v_s / world / peaks["bf16_tflops_sustained"],
+                     "frac_of_burst_peak": v_s / world / peaks["bf16_tflops"],
+                     "clocks": clocks_s,
+                     "gpu_launches": int(round(launches_per_step * n_sus))}
 
     # End to end through the C ABI with host buffers.  Every step uploads its
     # inputs (the block: X and dZ; a linear layer: X and dY) from pinned host
@@ -957,7 +1010,8 @@ def run_ours(args, torch):
                                      "source": peak_src,
                                      "theoretical": (value / world / theo["tflops"]) if theo else None,
                                      "theoretical_peak": theo},
-                "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "kernels": kernels, "sustained": sustained,
+                "cpu_baseline": cpu, "e2e": e2e,
                 "cublas_reference": cublas,
                 "clocks": clocks, "gpu_launches": int(sum(kcount.values())),
                 "cuda_graph": bool(args.graph),
