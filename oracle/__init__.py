@@ -61,7 +61,11 @@ def _configure(lib):
     lib.oracle_backward.argtypes = dims + [_dp, _dpp, _dpp, _dpp, _dpp, _dp,
                                            _dpp, _dp, _dpp, _dp, _dpp, _dp]
     lib.oracle_rows.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp, _dp,
-                                       _i64, ctypes.POINTER(_i64), _dp, _dp]
+                                       _i64, ctypes.POINTER(_i64), _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_sp_rows.argtypes = dims + [_dp, _dp, _dp, ctypes.c_double, _dpp, _dp, _dpp, _dp,
+                                          ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                          ctypes.c_double, _dp, _i64, ctypes.POINTER(_i64),
+                                          _dp, _dp]
     lib.oracle_cols.argtypes = dims + [_dp, _dpp, _dp, _dpp, _dp,
                                        _i64, ctypes.POINTER(_i64), _dp, _dp, _dp]
     lib.oracle_db2.argtypes = [_i64, _i64, _dp, _dp]
@@ -190,8 +194,10 @@ def forward_backward(X, A_shards, b1, B_shards, b2, dZ):
     return {**fw, **bw}
 
 
-def rows(X, A_shards, b1, B_shards, b2, dZ, row_idx):
-    """Z[r, :] and dX[r, :] for the selected token rows only."""
+def rows(X, A_shards, b1, B_shards, b2, dZ, row_idx, activations=False):
+    """Z[r, :] and dX[r, :] for the selected token rows only; with
+    activations=True also their rows of Y, H and dY ([len(rows), f] each, the
+    t shards side by side)."""
     lib = _load()
     X = _f64(X); dZ = _f64(dZ); b1 = _f64(b1); b2 = _f64(b2)
     A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
@@ -200,10 +206,16 @@ def rows(X, A_shards, b1, B_shards, b2, dZ, row_idx):
     if idx.size and (idx.min() < 0 or idx.max() >= T):
         raise IndexError("row index out of range")
     Zr = np.empty((idx.size, h)); dXr = np.empty((idx.size, h))
+    act = [np.empty((idx.size, f)) for _ in range(3)] if activations else None
+    null = ctypes.cast(None, _dp)
     pA, _ka = _ptrs(A); pB, _kb = _ptrs(B)
     lib.oracle_rows(T, h, f, t, _ptr(X), pA, _ptr(b1), pB, _ptr(b2), _ptr(dZ),
-                    idx.size, idx.ctypes.data_as(ctypes.POINTER(_i64)), _ptr(Zr), _ptr(dXr))
-    return {"Z": Zr, "dX": dXr}
+                    idx.size, idx.ctypes.data_as(ctypes.POINTER(_i64)), _ptr(Zr), _ptr(dXr),
+                    *([_ptr(a) for a in act] if act else [null, null, null]))
+    out = {"Z": Zr, "dX": dXr}
+    if act:
+        out.update(Y=act[0], H=act[1], dY=act[2])
+    return out
 
 
 def cols(X, A_shards, b1, B_shards, dZ, col_idx):
@@ -363,26 +375,64 @@ def layernorm(X, gamma, beta, eps: float, dXn=None):
     return out
 
 
-def sp_layer(X, gamma, beta, eps, A_shards, b1, B_shards, b2, p, seed, offset=0, dOut=None):
-    """Out = X + Dropout(MLP(LN(X))); with dOut the backward of every input:
-    dX (through both paths), dgamma, dbeta, dA_i, db1, dB_i, db2.  Also returns
-    the intermediates Xn, Z, keep."""
+def sp_block_inputs(X, gamma, beta, eps, p, seed, offset=0, dOut=None):
+    """The MLP block's inputs inside the sublayer: Xn = LN(X) (with the row
+    mean and rstd), the 0/1 keep mask as float64 [T, h], scale = 1 / (1 - p),
+    and with dOut given the block's upstream gradient dZ = dOut * keep * scale
+    (dropout backward)."""
     X = _f64(X)
     T, h = X.shape
     ln = layernorm(X, gamma, beta, eps)
     keep = dropout_keep(T, h, p, seed, offset).reshape(T, h).astype(np.float64)
     scale = 1.0 / (1.0 - float(p))
+    out = {"Xn": ln["Xn"], "mean": ln["mean"], "rstd": ln["rstd"], "keep": keep, "scale": scale}
+    if dOut is not None:
+        out["dZ"] = _f64(dOut) * keep * scale
+    return out
+
+
+def sp_layer(X, gamma, beta, eps, A_shards, b1, B_shards, b2, p, seed, offset=0, dOut=None):
+    """Out = X + Dropout(MLP(LN(X))); with dOut the backward of every input:
+    dX (through both paths), dgamma, dbeta, dA_i, db1, dB_i, db2.  Also returns
+    the intermediates Xn, Z, keep."""
+    X = _f64(X)
+    bi = sp_block_inputs(X, gamma, beta, eps, p, seed, offset, dOut)
+    keep, scale = bi["keep"], bi["scale"]
     if dOut is None:
-        blk = forward(ln["Xn"], A_shards, b1, B_shards, b2)
+        blk = forward(bi["Xn"], A_shards, b1, B_shards, b2)
         Out = X + keep * scale * blk["Z"]
-        return {"Out": Out, "Xn": ln["Xn"], "Z": blk["Z"], "keep": keep, "mean": ln["mean"],
-                "rstd": ln["rstd"]}
+        return {"Out": Out, "Xn": bi["Xn"], "Z": blk["Z"], "keep": keep, "mean": bi["mean"],
+                "rstd": bi["rstd"]}
     dOut = _f64(dOut)
-    dZ = dOut * keep * scale                      # dropout backward
-    blk = forward_backward(ln["Xn"], A_shards, b1, B_shards, b2, dZ)
+    dZ = bi["dZ"]                                 # dropout backward
+    blk = forward_backward(bi["Xn"], A_shards, b1, B_shards, b2, dZ)
     lnb = layernorm(X, gamma, beta, eps, dXn=blk["dX"])
     Out = X + keep * scale * blk["Z"]
-    return {"Out": Out, "Xn": ln["Xn"], "Z": blk["Z"], "keep": keep, "dZ": dZ,
+    return {"Out": Out, "Xn": bi["Xn"], "Z": blk["Z"], "keep": keep, "dZ": dZ,
             "dXn": blk["dX"], "dX": lnb["dX"] + dOut, "dgamma": lnb["dgamma"],
             "dbeta": lnb["dbeta"], "dA": blk["dA"], "db1": blk["db1"], "dB": blk["dB"],
-            "db2": blk["db2"], "mean": ln["mean"], "rstd": ln["rstd"]}
+            "db2": blk["db2"], "mean": bi["mean"], "rstd": bi["rstd"]}
+
+
+def sp_rows(X, gamma, beta, eps, A_shards, b1, B_shards, b2, p, seed, offset, dOut, row_idx):
+    """Out[r, :] and dX[r, :] of :func:`sp_layer` for the selected token rows
+    only (each row of the sublayer depends only on that row's inputs; the mask
+    of element (r, n) is fixed by its index r * h + n)."""
+    lib = _load()
+    X = _f64(X); gamma = _f64(gamma); beta = _f64(beta); dOut = _f64(dOut)
+    b1 = _f64(b1); b2 = _f64(b2)
+    A = [_f64(a) for a in A_shards]; B = [_f64(b) for b in B_shards]
+    T, h, f, t, fi = _check_shards(X, A, b1, B, b2)
+    if gamma.shape != (h,) or beta.shape != (h,) or dOut.shape != (T, h):
+        raise ValueError("gamma, beta must be [h] and dOut [T, h]")
+    idx = np.ascontiguousarray(np.asarray(row_idx, dtype=np.int64))
+    if idx.size and (idx.min() < 0 or idx.max() >= T):
+        raise IndexError("row index out of range")
+    scale = 1.0 / (1.0 - float(p))
+    Outr = np.empty((idx.size, h)); dXr = np.empty((idx.size, h))
+    pA, _ka = _ptrs(A); pB, _kb = _ptrs(B)
+    lib.oracle_sp_rows(T, h, f, t, _ptr(X), _ptr(gamma), _ptr(beta), float(eps), pA, _ptr(b1),
+                       pB, _ptr(b2), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                       dropout_threshold(p), scale, _ptr(dOut), idx.size,
+                       idx.ctypes.data_as(ctypes.POINTER(_i64)), _ptr(Outr), _ptr(dXr))
+    return {"Out": Outr, "dX": dXr}

@@ -52,6 +52,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -247,7 +248,9 @@ void oracle_backward(int64_t T, int64_t h, int64_t f, int t,
  *
  * oracle_rows: for each selected token row r = rows[q]:
  *   Zr[q, :]  = Z[r, :]   and   dXr[q, :] = dX[r, :]
- * (needs row r of Y_i, H_i and dY_i for every shard, computed here).
+ * (needs row r of Y_i, H_i and dY_i for every shard, computed here).  When
+ * Yr, Hr, dYr are not NULL they receive those rows too, shard after shard:
+ *   Yr[q, i*fi + j] = Y_i[r, j], likewise H_i and dY_i   ([nrows, f] each).
  */
 void oracle_rows(int64_t T, int64_t h, int64_t f, int t,
                  const double *X,
@@ -255,7 +258,8 @@ void oracle_rows(int64_t T, int64_t h, int64_t f, int t,
                  const double *const *B, const double *b2,
                  const double *dZ,
                  int64_t nrows, const int64_t *rows,
-                 double *Zr, double *dXr) {
+                 double *Zr, double *dXr,
+                 double *Yr, double *Hr, double *dYr) {
     const int64_t fi = f / t;
     (void)T;
     #pragma omp parallel for schedule(dynamic)
@@ -276,6 +280,9 @@ void oracle_rows(int64_t T, int64_t h, int64_t f, int t,
                 const double dy = dh * oracle_gelu_grad(y);
                 for (int64_t n = 0; n < h; ++n) z[n] += hv * Bi[j * h + n];
                 for (int64_t k = 0; k < h; ++k) dx[k] += dy * Ai[k * fi + j];
+                if (Yr) Yr[q * f + i * fi + j] = y;
+                if (Hr) Hr[q * f + i * fi + j] = hv;
+                if (dYr) dYr[q * f + i * fi + j] = dy;
             }
         }
         for (int64_t n = 0; n < h; ++n) z[n] += b2[n];
@@ -574,5 +581,51 @@ void oracle_layernorm_backward(int64_t T, int64_t h, const double *X, const doub
         }
         dgamma[n] = sgm;
         dbeta[n] = sbt;
+    }
+}
+
+/* ---- sampled rows of the sequence-parallel sublayer ---------------------
+ * Out[r, :] and dX[r, :] of Out = X + Dropout(MLP(LN(X))) for the selected
+ * token rows r = rows[q] of a [T, h] problem, with upstream gradient dOut.
+ * Every quantity of a token row depends only on that row (LayerNorm is over
+ * h, the mask of element (r, n) is fixed by its index r * h + n), so each row
+ * is the composition, in order, of the definitions above applied to one row:
+ *   LN forward of X[r]                     -> xn, mean, rstd
+ *   keep[n] of element r * h + n
+ *   dz = dOut[r] * keep * scale             (dropout backward)
+ *   the block on the one-row input xn      -> z, dxn  (oracle_rows)
+ *   Out[r] = X[r] + keep * scale * z
+ *   LN backward of X[r] for dxn, plus dOut[r] (the residual path)
+ * scale = 1 / (1 - p) and thresh = floor((1 - p) * 2^32) come from the caller.
+ */
+void oracle_sp_rows(int64_t T, int64_t h, int64_t f, int t,
+                    const double *X, const double *gamma, const double *beta, double eps,
+                    const double *const *A, const double *b1,
+                    const double *const *B, const double *b2,
+                    uint64_t seed, uint64_t offset, uint64_t thresh, double scale,
+                    const double *dOut, int64_t nrows, const int64_t *rows,
+                    double *Outr, double *dXr) {
+    (void)T;
+    #pragma omp parallel for schedule(dynamic)
+    for (int64_t q = 0; q < nrows; ++q) {
+        const int64_t r = rows[q];
+        const double *xr = X + r * h;
+        const double *dor = dOut + r * h;
+        double *buf = (double *)malloc(sizeof(double) * (size_t)(7 * h + 2));
+        uint8_t *keep = (uint8_t *)malloc((size_t)h);
+        if (!buf || !keep) { free(buf); free(keep); continue; }
+        double *xn = buf, *dz = buf + h, *zr = buf + 2 * h, *dxn = buf + 3 * h;
+        double *dxl = buf + 4 * h, *dgb = buf + 5 * h;  /* this row's dgamma, dbeta (unused) */
+        double *stats = buf + 7 * h;                     /* mean, rstd */
+        const int64_t zero = 0;
+        oracle_layernorm_forward(1, h, xr, gamma, beta, eps, xn, &stats[0], &stats[1]);
+        oracle_dropout_keep(seed, offset, thresh, r * h, h, keep);
+        for (int64_t n = 0; n < h; ++n) dz[n] = dor[n] * (double)keep[n] * scale;
+        oracle_rows(1, h, f, t, xn, A, b1, B, b2, dz, 1, &zero, zr, dxn, NULL, NULL, NULL);
+        for (int64_t n = 0; n < h; ++n) Outr[q * h + n] = xr[n] + (double)keep[n] * scale * zr[n];
+        oracle_layernorm_backward(1, h, xr, gamma, &stats[0], &stats[1], dxn, dxl, dgb, dgb + h);
+        for (int64_t n = 0; n < h; ++n) dXr[q * h + n] = dxl[n] + dor[n];
+        free(buf);
+        free(keep);
     }
 }

@@ -78,20 +78,51 @@ def sample_indices(n: int, k: int, seed: int) -> np.ndarray:
     return np.array(sorted(pick), dtype=np.int64)
 
 
+def tile_samples(n: int, seed: int, tile: int = 256, half: int = 128) -> np.ndarray:
+    """Indices in [0, n) that reach every tile of the GEMMs along one axis:
+    one seeded index in each `half`-wide half of every `tile`-wide tile (the
+    two CTAs of a pair tile, or the two halves of an output tile's columns),
+    plus the first and the last index."""
+    rng = np.random.default_rng(seed)
+    pick = {0, n - 1} if n > 0 else set()
+    for lo in range(0, n, half):
+        hi = min(n, lo + half)
+        pick.add(int(rng.integers(lo, hi)))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def shard_tile_samples(f: int, t: int, seed: int) -> np.ndarray:
+    """Global ffn columns that reach every 256-wide tile of every shard's
+    [*, f/t] GEMM outputs (one in each 128-wide half), as i * f/t + j."""
+    fi = f // t
+    out = [i * fi + tile_samples(fi, seed + i) for i in range(t)]
+    return np.concatenate(out).astype(np.int64)
+
+
 def compare_sampled(block, inputs: dict, w, oracle_mod, rows: np.ndarray, cols: np.ndarray,
-                    report: dict | None = None):
-    """Sampled outputs computed one by one by the oracle: Z/dX rows, dA
-    columns, dB rows, db1 entries; db2 in full."""
+                    report: dict | None = None, intermediates: bool = True):
+    """Sampled outputs computed one by one by the oracle: rows of Z, dX and
+    (intermediates=True) of the saved Y, H, dY; dA columns, dB rows and db1
+    entries at the sampled ffn columns; db2 in full."""
     from tensor_transformer_mlp_gemm_gb300.inputs import column_shards, row_shards
     torch.cuda.synchronize()
     A = column_shards(inputs["A"], w.t)
     B = row_shards(inputs["B"], w.t)
-    r = oracle_mod.rows(inputs["X"], A, inputs["b1"], B, inputs["b2"], inputs["dZ"], rows)
+    r = oracle_mod.rows(inputs["X"], A, inputs["b1"], B, inputs["b2"], inputs["dZ"], rows,
+                        activations=intermediates)
     c = oracle_mod.cols(inputs["X"], A, inputs["b1"], B, inputs["dZ"], cols)
+    ridx = torch.from_numpy(rows)
     Z = cat(block.Z, 0)
     dX = cat(block.dX, 0)
-    gate("Z[rows]", Z[rows], r["Z"], report)
-    gate("dX[rows]", dX[rows], r["dX"], report)
+    gate("Z[rows]", Z[ridx], r["Z"], report)
+    gate("dX[rows]", dX[ridx], r["dX"], report)
+    if intermediates:
+        sv = block.saved()
+        dev = sv["Y"][0].device
+        gidx = ridx.to(dev)
+        for name in ("Y", "H", "dY"):
+            got = torch.cat([x.index_select(0, gidx).cpu() for x in sv[name]], dim=1)
+            gate(f"{name}[rows]", got, r[name], report)
     fi = w.ffn // w.t
     dA_cols = torch.stack([block.dA[int(q) // fi][:, int(q) % fi].cpu() for q in cols])
     dB_rows = torch.stack([block.dB[int(q) // fi][int(q) % fi, :].cpu() for q in cols])

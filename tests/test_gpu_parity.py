@@ -1,10 +1,14 @@
 """Parity of the CUDA path (through the C ABI) against the fp64 oracle.
 
 Small and ragged problems are compared element by element against the full
-oracle; the full-size workloads (the 175B-class layer and the
-sequence-parallel one) are compared on sampled rows/columns that the oracle
-computes one by one, plus exact GPU-side invariants: sharded == unsharded and
-sequence-parallel == plain, bitwise.
+oracle; the full-size workloads (the 1.3B-, 175B-class and sequence-parallel
+layers) are compared on sampled rows/columns that the oracle computes one by
+one, chosen so that every tile of every GEMM is reached: a token row in each
+128-row half of every 256-row pair tile (rows of Z, dX and the saved Y, H,
+dY), and an ffn column in each 128-wide half of every 256-wide output tile of
+every shard (columns of dA, rows of dB, entries of db1); db2 in full.  Exact
+GPU-side invariants ride along: sharded == unsharded and sequence-parallel ==
+plain, bitwise.
 """
 import os
 
@@ -13,7 +17,7 @@ import pytest
 import torch
 
 import oracle
-from parity import compare_full, compare_sampled, sample_indices
+from parity import compare_full, compare_sampled, shard_tile_samples, tile_samples
 from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
                                                       make_inputs, row_shards)
 
@@ -94,9 +98,8 @@ def test_gpt_1p3b_sharded_equals_unsharded():
     assert torch.equal(torch.cat(b4.dA, 1), b1.dA[0])
     assert torch.equal(torch.cat(b4.dB, 0), b1.dB[0])
     assert torch.equal(b4.db1, b1.db1) and torch.equal(b4.db2, b1.db2)
-    rows = sample_indices(w4.tokens, 12, 5)
-    cols = sample_indices(w4.ffn, 24, 6)
-    compare_sampled(b4, inputs, w4, oracle, rows, cols)
+    compare_sampled(b4, inputs, w4, oracle, tile_samples(w4.tokens, 5),
+                    shard_tile_samples(w4.ffn, w4.t, 6))
 
 
 def test_gpt_175b_sampled():
@@ -105,8 +108,9 @@ def test_gpt_175b_sampled():
     blk = _block(w, inputs)
     blk.step()
     torch.cuda.synchronize()
-    rows = sample_indices(w.tokens, 8, 7)
-    cols = sample_indices(w.ffn, 16, 8)
+    rows = tile_samples(w.tokens, 7)
+    cols = shard_tile_samples(w.ffn, w.t, 8)
+    assert len(rows) >= 2 * (w.tokens // 256) and len(cols) >= 2 * (w.ffn // 256)
     compare_sampled(blk, inputs, w, oracle, rows, cols)
     # the same step again gives the same bits
     Z0 = [z.clone() for z in blk.Z]
@@ -123,9 +127,8 @@ def test_sequence_parallel_sampled_and_equal_to_plain():
     sp = _block(w, inputs)
     sp.step()
     torch.cuda.synchronize()
-    rows = sample_indices(w.tokens, 8, 9)
-    cols = sample_indices(w.ffn, 16, 10)
-    compare_sampled(sp, inputs, w, oracle, rows, cols)
+    compare_sampled(sp, inputs, w, oracle, tile_samples(w.tokens, 9),
+                    shard_tile_samples(w.ffn, w.t, 10))
     from dataclasses import replace
     plain = _block(replace(w, seq_chunks=1), inputs)
     plain.step()

@@ -5,11 +5,12 @@ oracle.
 Small and ragged layers are compared element by element against the full
 oracle, and the dropout mask exactly (every element the oracle drops is an
 exact zero of the GPU's dZ, and only those).  The 16384 x 4096 sequence-
-parallel workload is compared on sampled rows (Out, dX: each row depends only
-on its own inputs; the mask is taken at the rows' global element indices) and
-sampled columns of the weight gradients (from the oracle's full LN(X) and dZ);
-LayerNorm's dgamma and dbeta are checked element by element at the small
-sizes only.
+parallel workload is compared on sampled rows (Out, dX from the oracle's
+sampled sublayer rows, sp_rows: one row in each 128-row half of every 256-row
+pair tile) and sampled columns of the weight gradients (one in each 128-wide
+half of every 256-wide tile of every shard, from the block's inputs LN(X) and
+dZ inside the oracle's sublayer, sp_block_inputs); LayerNorm's dgamma and
+dbeta are checked element by element at the small sizes only.
 """
 import os
 
@@ -18,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from parity import gate, sample_indices
+from parity import gate, shard_tile_samples, tile_samples
 from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
                                                       make_sp_inputs, row_shards)
 
@@ -121,37 +122,28 @@ def test_sp_h4096_sampled():
     lay = _layer(w, inputs, p, seed)
     lay.step()
     torch.cuda.synchronize()
-    T, h = w.tokens, w.hidden
     rep = {}
-    X, dOut = inputs["X"], inputs["dZ"]
     A, B = column_shards(inputs["A"], w.t), row_shards(inputs["B"], w.t)
-    scale = 1.0 / (1.0 - p)
-    rows = sample_indices(T, 8, 31)
-    keep_r = np.stack([oracle.dropout_keep(T, h, p, seed, 0, e0=int(r) * h, count=h)
-                       for r in rows]).astype(np.float64)
-    ln = oracle.layernorm(X[rows], inputs["gamma"], inputs["beta"], EPS)
-    dZ_r = dOut[rows].double().numpy() * keep_r * scale
-    fb = oracle.forward_backward(ln["Xn"], A, inputs["b1"], B, inputs["b2"], dZ_r)
-    Out_r = X[rows].double().numpy() + keep_r * scale * fb["Z"]
-    lnb = oracle.layernorm(X[rows], inputs["gamma"], inputs["beta"], EPS, dXn=fb["dX"])
-    dX_r = lnb["dX"] + dOut[rows].double().numpy()
+    # a token row in each 128-row half of every 256-row pair tile
+    rows = tile_samples(w.tokens, 31)
+    r = oracle.sp_rows(inputs["X"], inputs["gamma"], inputs["beta"], EPS, A, inputs["b1"], B,
+                       inputs["b2"], p, seed, 0, inputs["dZ"], rows)
     Out = torch.cat(lay.Out, 0)
     dX = torch.cat(lay.dX, 0)
     idx = torch.from_numpy(rows).to(Out.device)
-    gate("Out[rows]", Out[idx].cpu(), Out_r, rep)
-    gate("dX[rows]", dX[idx].cpu(), dX_r, rep)
-    # weight-gradient columns from the full LN(X) and dZ
-    Xn = oracle.layernorm(X, inputs["gamma"], inputs["beta"], EPS)["Xn"]
-    keep = oracle.dropout_keep(T, h, p, seed).reshape(T, h)
-    dZ = dOut.double().numpy() * keep * scale
-    del keep
-    cols = sample_indices(w.ffn, 12, 32)
-    c = oracle.cols(Xn, A, inputs["b1"], B, dZ, cols)
+    gate("Out[rows]", Out[idx].cpu(), r["Out"], rep)
+    gate("dX[rows]", dX[idx].cpu(), r["dX"], rep)
+    # weight-gradient columns (both halves of every 256-wide tile of every
+    # shard) from the block's inputs inside the sublayer
+    bi = oracle.sp_block_inputs(inputs["X"], inputs["gamma"], inputs["beta"], EPS, p, seed, 0,
+                                dOut=inputs["dZ"])
+    cols = shard_tile_samples(w.ffn, w.t, 32)
+    c = oracle.cols(bi["Xn"], A, inputs["b1"], B, bi["dZ"], cols)
     fi = w.ffn // w.t
     gate("dA[:,cols]", torch.stack([lay.dA[int(q) // fi][:, int(q) % fi].cpu() for q in cols]),
          c["dA_cols"], rep)
     gate("dB[cols,:]", torch.stack([lay.dB[int(q) // fi][int(q) % fi, :].cpu() for q in cols]),
          c["dB_rows"], rep)
     gate("db1[cols]", lay.db1.cpu()[cols], c["db1"], rep)
-    gate("db2", lay.db2, oracle.db2(dZ), rep)
+    gate("db2", lay.db2, oracle.db2(bi["dZ"]), rep)
     _report(rep)

@@ -273,9 +273,14 @@ def test_sampled_rows_and_cols_equal_full():
     As, Bs = _split_cols(A, t), _split_rows(B, t)
     full = oracle.forward_backward(X, As, b1, Bs, b2, dZ)
     rows = [0, 7, 19, 3]
-    r = oracle.rows(X, As, b1, Bs, b2, dZ, rows)
+    r = oracle.rows(X, As, b1, Bs, b2, dZ, rows, activations=True)
     assert np.array_equal(r["Z"], full["Z"][rows])
     assert np.array_equal(r["dX"], full["dX"][rows])
+    assert np.array_equal(r["Y"], _cat(full["Y"], 1)[rows])
+    assert np.array_equal(r["H"], _cat(full["H"], 1)[rows])
+    assert np.array_equal(r["dY"], _cat(full["dY"], 1)[rows])
+    plain = oracle.rows(X, As, b1, Bs, b2, dZ, rows)
+    assert set(plain) == {"Z", "dX"} and np.array_equal(plain["Z"], r["Z"])
     cols = [0, 15, 16, 47, 30]
     c = oracle.cols(X, As, b1, Bs, dZ, cols)
     dA, dB = _cat(full["dA"], 1), _cat(full["dB"], 0)

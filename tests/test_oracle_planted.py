@@ -58,6 +58,12 @@ MUTATIONS = [
     ("layernorm backward: mean term dropped", "dX[r * h + n] = rstd[r] * (dy[n] * gamma[n] - mg - xh * mgx);",
      "dX[r * h + n] = rstd[r] * (dy[n] * gamma[n] - xh * mgx);"),
     ("layernorm backward: dgamma without xhat", "sgm += dXn[r * h + n] * xh;", "sgm += dXn[r * h + n];"),
+    # sampled rows (full-size parity)
+    ("sampled rows: H holds the pre-activation", "if (Hr) Hr[q * f + i * fi + j] = hv;",
+     "if (Hr) Hr[q * f + i * fi + j] = y;"),
+    ("sampled sublayer rows: mask of the sample index, not the token row",
+     "oracle_dropout_keep(seed, offset, thresh, r * h, h, keep);",
+     "oracle_dropout_keep(seed, offset, thresh, q * h, h, keep);"),
 ]
 
 PIN_CALLS = [
@@ -74,6 +80,8 @@ PIN_CALLS = [
     lambda: sp.test_layernorm_moments_and_affine_invariance(),
     lambda: sp.test_layernorm_backward_finite_differences(),
     lambda: sp.test_sp_layer_backward_finite_differences(),
+    lambda: pins.test_sampled_rows_and_cols_equal_full(),
+    lambda: sp.test_sp_rows_equal_sp_layer_bitwise(24, 16, 32, 2, 0.3, 5),
 ]
 
 

@@ -19,7 +19,10 @@ What pins what:
     of the input; central finite differences for dX, dgamma, dbeta;
   * the sublayer: Out - X = keep / (1 - p) * MLP(LN(X)); central finite
     differences of sum(dOut * Out) for X (both paths), gamma, beta, b2 and
-    one weight entry, with the mask held fixed.
+    one weight entry, with the mask held fixed;
+  * the sublayer's sampled rows (sp_rows, used at full size): bitwise equal
+    to the same rows of the whole pinned sublayer, for several dropout rates,
+    mask offsets, shard counts and row orders.
 """
 import numpy as np
 import pytest
@@ -173,3 +176,26 @@ def test_sp_layer_backward_finite_differences():
     def ma(d):
         A2 = [a.copy() for a in A]; A2[1][2, 3] += d; return {"A_": A2}
     assert abs(fd(ma) - r["dA"][1][2, 3]) < 1e-6
+
+
+@pytest.mark.parametrize("T,h,f,t,p,offset", [
+    (24, 16, 32, 2, 0.3, 5),
+    (9, 8, 24, 3, 0.0, 0),
+    (40, 12, 16, 1, 0.5, 123),
+])
+def test_sp_rows_equal_sp_layer_bitwise(T, h, f, t, p, offset):
+    rng = np.random.default_rng(T * 31 + h)
+    X = rng.standard_normal((T, h))
+    A = rng.standard_normal((h, f)) * 0.3
+    B = rng.standard_normal((f, h)) * 0.3
+    b1 = rng.standard_normal(f) * 0.1
+    b2 = rng.standard_normal(h) * 0.1
+    dOut = rng.standard_normal((T, h))
+    gamma = 1.0 + 0.1 * rng.standard_normal(h)
+    beta = 0.1 * rng.standard_normal(h)
+    As, Bs = _split_cols(A, t), _split_rows(B, t)
+    full = oracle.sp_layer(X, gamma, beta, 1e-5, As, b1, Bs, b2, p, 77, offset, dOut=dOut)
+    rows = [0, T - 1, T // 2, 1, T // 3]
+    got = oracle.sp_rows(X, gamma, beta, 1e-5, As, b1, Bs, b2, p, 77, offset, dOut, rows)
+    assert np.array_equal(got["Out"], full["Out"][rows])
+    assert np.array_equal(got["dX"], full["dX"][rows])
