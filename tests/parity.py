@@ -68,16 +68,6 @@ def compare_full(block, ref: dict, report: dict | None = None, intermediates: bo
     gate("db2", block.db2, ref["db2"], report)
 
 
-def sample_indices(n: int, k: int, seed: int) -> np.ndarray:
-    """k distinct indices in [0, n): the first, the last, and seeded others."""
-    rng = np.random.default_rng(seed)
-    k = min(k, n)
-    pick = {0, n - 1}
-    while len(pick) < k:
-        pick.add(int(rng.integers(0, n)))
-    return np.array(sorted(pick), dtype=np.int64)
-
-
 def tile_samples(n: int, seed: int, tile: int = 256, half: int = 128) -> np.ndarray:
     """Indices in [0, n) that reach every tile of the GEMMs along one axis:
     one seeded index in each `half`-wide half of every `tile`-wide tile (the

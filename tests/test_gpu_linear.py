@@ -18,7 +18,8 @@ import pytest
 import torch
 
 import oracle
-from parity import gate, sample_indices
+from guard import GuardBands
+from parity import gate, shard_tile_samples, tile_samples
 from tensor_transformer_mlp_gemm_gb300.inputs import (LINEAR_WORKLOADS, column_shards, custom,
                                                       custom_linear, make_inputs,
                                                       make_linear_inputs, row_shards)
@@ -67,9 +68,13 @@ def _oracle(w, X, W, b, dY):
 def _run_full(w, seed=0):
     inputs = make_linear_inputs(w, seed)
     lin = _layer(w, inputs)
+    g = GuardBands()
+    g.guard(lin, ["Y", "dX", "dW", "db", "ws"])
+    g.watch_inputs(lin, ["X", "W", "b", "dY"])
     lin.step()
     from tensor_transformer_mlp_gemm_gb300 import binding
     assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    g.check()
     got = _full(lin)
     ref = _oracle(w, inputs["X"], inputs["W"], inputs["b"], inputs["dY"])
     for k in ("Y", "dX", "dW", "db"):
@@ -191,6 +196,18 @@ def _sampled(w, inputs, lin, rows, cols):
     gate("db[cols]", lin.db.cpu()[cols], c["db"])
 
 
+def _tile_covering(w, seed):
+    """Token rows in both 128-row halves of every 256-row pair tile, and output
+    columns in both 128-wide halves of every 256-wide tile (of every shard, for
+    the column-parallel layer's sharded output)."""
+    rows = tile_samples(w.tokens, seed)
+    if w.split == "column":
+        cols = shard_tile_samples(w.out_features, w.t, seed + 1)
+    else:
+        cols = tile_samples(w.out_features, seed + 1)
+    return torch.from_numpy(rows), torch.from_numpy(cols)
+
+
 @pytest.mark.parametrize("name", ["qkv_175b", "attn_out_175b"])
 def test_175b_projections_sampled(name):
     w = LINEAR_WORKLOADS[name]
@@ -198,8 +215,7 @@ def test_175b_projections_sampled(name):
     lin = _layer(w, inputs)
     lin.step()
     torch.cuda.synchronize()
-    rows = torch.from_numpy(sample_indices(w.tokens, 8, 21))
-    cols = torch.from_numpy(sample_indices(w.out_features, 16, 22))
+    rows, cols = _tile_covering(w, 21)
     _sampled(w, inputs, lin, rows, cols)
     Y0, dW0 = [y.clone() for y in lin.Y], lin.dW[5].clone()
     lin.step()
@@ -216,8 +232,7 @@ def test_sequence_parallel_sampled_and_equal_to_plain(name):
     sp = _layer(w, inputs)
     sp.step()
     torch.cuda.synchronize()
-    rows = torch.from_numpy(sample_indices(w.tokens, 8, 23))
-    cols = torch.from_numpy(sample_indices(w.out_features, 16, 24))
+    rows, cols = _tile_covering(w, 23)
     _sampled(w, inputs, sp, rows, cols)
     plain = _layer(replace(w, seq_chunks=1), inputs)
     plain.step()

@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from guard import GuardBands
 from parity import compare_full, compare_sampled, shard_tile_samples, tile_samples
 from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
                                                       make_inputs, row_shards)
@@ -45,9 +46,15 @@ def _oracle_full(w, inputs):
 def _run_full(w, seed=0):
     inputs = make_inputs(w, seed)
     blk = _block(w, inputs)
+    # every output and the workspace inside sentinel-filled guard bands; the
+    # inputs must come back unchanged
+    g = GuardBands()
+    g.guard(blk, ["Z", "dX", "dA", "dB", "db1", "db2", "ws"])
+    g.watch_inputs(blk, ["X", "dZ", "A", "B", "b1", "b2"])
     blk.step()
     from tensor_transformer_mlp_gemm_gb300 import binding
     assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    g.check()
     ref = _oracle_full(w, inputs)
     compare_full(blk, ref)
     return blk

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from guard import GuardBands
 from parity import compare_full, gate
 from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
                                                       make_inputs, row_shards)
@@ -38,8 +39,12 @@ def test_recompute_against_oracle(w):
     from tensor_transformer_mlp_gemm_gb300 import binding
     inputs = make_inputs(w, 21)
     blk = _block(w, inputs, recompute=True)
+    g = GuardBands()
+    g.guard(blk, ["Z", "dX", "dA", "dB", "db1", "db2", "saved_y", "scratch"])
+    g.watch_inputs(blk, ["X", "dZ", "A", "B", "b1", "b2"])
     blk.step()
     assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    g.check()
     ref = oracle.forward_backward(inputs["X"], column_shards(inputs["A"], w.t), inputs["b1"],
                                   row_shards(inputs["B"], w.t), inputs["b2"], inputs["dZ"])
     compare_full(blk, ref)  # H here is the copy rebuilt by the backward pass

@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from guard import GuardBands
 from parity import gate, shard_tile_samples, tile_samples
 from tensor_transformer_mlp_gemm_gb300.inputs import (WORKLOADS, column_shards, custom,
                                                       make_sp_inputs, row_shards)
@@ -53,9 +54,13 @@ def _run_full(w, p, seed=0):
     rep = {}
     inputs = make_sp_inputs(w, seed)
     lay = _layer(w, inputs, p)
+    g = GuardBands()
+    g.guard(lay, ["Out", "dX", "dA", "dB", "db1", "db2", "dgamma", "dbeta", "ws"])
+    g.watch_inputs(lay, ["X", "dOut", "A", "B", "b1", "b2", "gamma", "beta"])
     lay.step()
     from tensor_transformer_mlp_gemm_gb300 import binding
     assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    g.check()
     ref = oracle.sp_layer(inputs["X"], inputs["gamma"], inputs["beta"], EPS,
                           column_shards(inputs["A"], w.t), inputs["b1"],
                           row_shards(inputs["B"], w.t), inputs["b2"], p, 1234, dOut=inputs["dZ"])
