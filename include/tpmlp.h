@@ -332,6 +332,25 @@ tpmlp_status tpmlp_set_split_min_kblocks(int kblocks);
  * it.  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_head_prefetch(int kblocks);
 
+/* TMA tensor-map cache.  Every call encodes one tensor map per operand shard,
+ * token chunk and output of each GEMM it launches; the library keeps the
+ * encoded maps in a cache keyed by every argument of the encoding (base
+ * address, element type, extents, strides, box, swizzle), so a repeated call
+ * on the same buffers encodes nothing.  A buffer at a new address is a new key
+ * (a stale entry is never used for another address).  At most 4096 maps are
+ * kept; when the cache is full it is emptied.  Thread-safe (one mutex).
+ * tpmlp_map_cache_stats reports the hits, misses (encodings) and entries so
+ * far; any pointer may be NULL.  Always TPMLP_OK. */
+tpmlp_status tpmlp_map_cache_stats(uint64_t* hits, uint64_t* misses, uint64_t* entries);
+
+/* Self-test of the cache logic on the host (no GPU, no driver): runs a fixed
+ * sequence against a private cache of capacity 4 with a stand-in encoder and
+ * writes out[0..7] = hits, misses, encoder calls, final entries, 1 if a hit
+ * returned the bytes of the first encoding, 1 if a new address gave another
+ * map, the capacity, and the key size in bytes.  n >= 8, else
+ * TPMLP_ERR_INVALID_ARG. */
+tpmlp_status tpmlp_selftest_map_cache(uint64_t* out, int n);
+
 /* Upper bound, in nanoseconds, on any single wait inside a kernel of this
  * library (default 2e9).  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);

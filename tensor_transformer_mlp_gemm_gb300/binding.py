@@ -39,7 +39,7 @@ EXPORTED = (
     "tpmlp_linear_workspace_bytes", "tpmlp_column_linear_forward", "tpmlp_column_linear_backward",
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
     "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
-    "tpmlp_set_head_prefetch",
+    "tpmlp_set_head_prefetch", "tpmlp_map_cache_stats", "tpmlp_selftest_map_cache",
 )
 
 
@@ -88,6 +88,11 @@ _lib.tpmlp_forward_recompute.argtypes = [_dims_p, _vpp, _vpp, _vp, _vpp, _vp, ct
 _lib.tpmlp_backward_recompute.restype = ctypes.c_int
 _lib.tpmlp_backward_recompute.argtypes = [_dims_p, _vpp, _vpp, _vpp, _vpp, _vp, _vp, _vpp, _vpp,
                                           _vp, _vpp, _vp, _vp]
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+_lib.tpmlp_map_cache_stats.restype = ctypes.c_int
+_lib.tpmlp_map_cache_stats.argtypes = [_u64p, _u64p, _u64p]
+_lib.tpmlp_selftest_map_cache.restype = ctypes.c_int
+_lib.tpmlp_selftest_map_cache.argtypes = [_u64p, ctypes.c_int]
 _lib.tpmlp_status_string.restype = ctypes.c_char_p
 _lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 _lib.tpmlp_sync_check.restype = ctypes.c_int
@@ -242,6 +247,22 @@ def tpmlp_set_split_min_kblocks(kblocks: int) -> None:
 
 def tpmlp_set_head_prefetch(kblocks: int) -> None:
     _check(_lib.tpmlp_set_head_prefetch(int(kblocks)), "tpmlp_set_head_prefetch")
+
+
+def tpmlp_map_cache_stats() -> dict:
+    """Hits, misses (encodings) and entries of the library's tensor-map cache."""
+    v = [ctypes.c_uint64() for _ in range(3)]
+    _check(_lib.tpmlp_map_cache_stats(*[ctypes.byref(x) for x in v]), "tpmlp_map_cache_stats")
+    return {"hits": v[0].value, "misses": v[1].value, "entries": v[2].value}
+
+
+def tpmlp_selftest_map_cache() -> dict:
+    """The cache logic's host self-test (see include/tpmlp.h)."""
+    out = (ctypes.c_uint64 * 8)()
+    _check(_lib.tpmlp_selftest_map_cache(out, 8), "tpmlp_selftest_map_cache")
+    keys = ("hits", "misses", "encoder_calls", "entries", "hit_same_bytes", "new_address_differs",
+            "capacity", "key_bytes")
+    return dict(zip(keys, [int(x) for x in out]))
 
 
 def tpmlp_set_wait_timeout_ns(ns: int) -> None:

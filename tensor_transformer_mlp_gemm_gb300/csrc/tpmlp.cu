@@ -34,6 +34,7 @@
 #include "block_internal.h"
 #include "colsum.cuh"
 #include "gemm_params.h"
+#include "map_cache.h"
 #include "tpmlp.h"
 
 #define TPMLP_API extern "C" __attribute__((visibility("default")))
@@ -111,6 +112,23 @@ tpmlp_status device_info(DeviceInfo** out) {
 }
 
 // ---- tensor maps -------------------------------------------------------------------------
+// Every map goes through the cache: encoded once per (address, shape, box,
+// swizzle), then copied.
+constexpr size_t kMapCacheCapacity = 4096;
+MapCache g_maps(kMapCacheCapacity);
+
+static bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t rank, const void* ptr,
+                         const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                         CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2promo) {
+    const MapKey key = make_map_key(dtype, rank, ptr, dims, strides, box, swizzle, l2promo);
+    return g_maps.get(key, m, [&](CUtensorMap* out) {
+        const cuuint32_t estr[3] = {1, 1, 1};
+        return g_encode(out, dtype, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2promo,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
+}
+
 // bf16 row-major matrix [outer, inner] with leading dimension ld (elements).
 //   K-major operand tile: box {BK, box_rows} (BK along the contiguous K axis)
 //   MN-major operand tile: box {64, BK}      (64 along the contiguous M/N axis)
@@ -119,11 +137,8 @@ static bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, int box_rows) {
@@ -143,11 +158,8 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, 
     cuuint64_t dims[3] = {MN_CHUNK, K, rows / MN_CHUNK};
     cuuint64_t strides[2] = {rows * 2, MN_CHUNK * 2};
     cuuint32_t box[3] = {MN_CHUNK, BK, static_cast<cuuint32_t>(BM / MN_CHUNK)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // Epilogue store map: row-major [rows, cols] output, box 32 x 32; fp32 boxes
@@ -157,13 +169,10 @@ bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, b
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * esize};
     cuuint32_t box[2] = {EPI_CHUNK, 32};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, ptr, dims, strides, box,
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 tpmlp_status check_ptrs(const void* const* arr, int n) {
@@ -209,10 +218,8 @@ bool attach_split(GemmParams& p, void* split_part, void* split_cnt) {
                           static_cast<cuuint64_t>(MAX_SPLIT_UNITS) * CLUSTER_M};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(BN) * 4};
     cuuint32_t box[2] = {EPI_CHUNK, 32};
-    cuuint32_t estr[2] = {1, 1};
-    if (g_encode(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, split_part, dims,
-                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!encode_tiled(&p.part_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, split_part, dims, strides,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE))
         return false;
     p.partial = reinterpret_cast<const float*>(split_part);
     p.counters = reinterpret_cast<int*>(split_cnt);
@@ -566,6 +573,67 @@ TPMLP_API tpmlp_status tpmlp_set_head_prefetch(int kblocks) {
     if (kblocks < 0 || kblocks > 64) return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     g_head_prefetch = kblocks;
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_map_cache_stats(uint64_t* hits, uint64_t* misses,
+                                              uint64_t* entries) {
+    g_maps.stats(hits, misses, entries);
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_selftest_map_cache(uint64_t* out, int n) {
+    // A private cache of capacity 4 with a stand-in encoder (no driver, no
+    // GPU): the map's bytes are a function of its key, and each encoder call
+    // is counted.
+    if (!out || n < 8) return TPMLP_ERR_INVALID_ARG;
+    MapCache cache(4);
+    uint64_t calls = 0;
+    auto fake = [&](const MapKey& k, CUtensorMap* m) {
+        return cache.get(k, m, [&](CUtensorMap* o) {
+            ++calls;
+            std::memset(o, 0, sizeof(*o));
+            std::memcpy(o, &k, sizeof(k) < sizeof(*o) ? sizeof(k) : sizeof(*o));
+            return true;
+        });
+    };
+    alignas(64) static char buf[4096];
+    cuuint64_t dims[2] = {1024, 512};
+    cuuint64_t strides[1] = {2048};
+    cuuint32_t box[2] = {64, 128};
+    const MapKey a = make_map_key(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, buf, dims, strides, box,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    const MapKey a_moved = make_map_key(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, buf + 256, dims,
+                                        strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    cuuint32_t box2[2] = {64, 256};
+    const MapKey a_box = make_map_key(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, buf, dims, strides, box2,
+                                      CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    CUtensorMap m1, m2, m3, m4;
+    fake(a, &m1);                                  // miss: encoded
+    fake(a, &m2);                                  // hit: same key, not encoded again
+    const bool same = std::memcmp(&m1, &m2, sizeof(m1)) == 0;
+    fake(a_moved, &m3);                            // miss: new address
+    fake(a_box, &m4);                              // miss: new box
+    const bool moved_differs = std::memcmp(&m1, &m3, sizeof(m1)) != 0;
+    for (int i = 0; i < 6; ++i) {                  // more keys than the capacity
+        const MapKey k = make_map_key(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, buf + 512 + 16 * i,
+                                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+        CUtensorMap m;
+        fake(k, &m);
+    }
+    uint64_t hits = 0, misses = 0, entries = 0;
+    cache.stats(&hits, &misses, &entries);
+    out[0] = hits;
+    out[1] = misses;
+    out[2] = calls;
+    out[3] = entries;
+    out[4] = same ? 1 : 0;
+    out[5] = moved_differs ? 1 : 0;
+    out[6] = 4;  // capacity
+    out[7] = sizeof(MapKey);
     return TPMLP_OK;
 }
 

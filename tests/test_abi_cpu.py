@@ -240,3 +240,19 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
                 assert "liboracle" not in text and "oracle.c" not in text, fn
+
+
+def test_tensor_map_cache_logic(binding):
+    """The tensor-map cache on the host: a repeated key is a hit with the same
+    bytes and no new encoding; a new address or box is a miss; the cache never
+    holds more than its capacity."""
+    r = binding.tpmlp_selftest_map_cache()
+    assert r["key_bytes"] == 80
+    # a, a (hit), a at a new address, a with a new box, then six new keys
+    assert r["hits"] == 1 and r["misses"] == 9 and r["encoder_calls"] == 9
+    assert r["hit_same_bytes"] == 1 and r["new_address_differs"] == 1
+    assert 1 <= r["entries"] <= r["capacity"]
+    lib = binding.library()
+    assert lib.tpmlp_selftest_map_cache(None, 8) == binding.TPMLP_ERR_INVALID_ARG
+    st = binding.tpmlp_map_cache_stats()
+    assert set(st) == {"hits", "misses", "entries"}

@@ -251,3 +251,28 @@ def test_head_prefetch_full_and_bitwise(T, h, f, t, chunks):
     _assert_bitwise(pf.dX, plain.dX, "dX")
     _assert_bitwise(pf.dA, plain.dA, "dA")
     _assert_bitwise(pf.dB, plain.dB, "dB")
+
+
+def test_tensor_map_cache_hits_on_repeat_and_misses_on_new_buffers():
+    """A repeated step on the same buffers encodes no tensor map; a block on
+    new buffers encodes its own; results do not depend on the cache."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    w = custom(333, 264, 1032, 3)
+    inputs = make_inputs(w, 15)
+    a = _block(w, inputs)
+    a.step()
+    torch.cuda.synchronize()
+    first = [z.clone() for z in a.Z] + [x.clone() for x in a.dA]
+    s0 = binding.tpmlp_map_cache_stats()
+    a.step()
+    torch.cuda.synchronize()
+    s1 = binding.tpmlp_map_cache_stats()
+    assert s1["misses"] == s0["misses"], "a repeated step encoded tensor maps"
+    assert s1["hits"] > s0["hits"]
+    _assert_bitwise(a.Z + a.dA, first, "repeat")
+    b = _block(w, inputs)
+    b.step()
+    torch.cuda.synchronize()
+    s2 = binding.tpmlp_map_cache_stats()
+    assert s2["misses"] > s1["misses"], "new buffers reused another buffer's maps"
+    _assert_bitwise(b.Z + b.dA, first, "new buffers")
