@@ -332,6 +332,19 @@ tpmlp_status tpmlp_set_split_min_kblocks(int kblocks);
  * it.  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_head_prefetch(int kblocks);
 
+/* Tile width of the GEMMs with bf16 outputs (every GEMM but the weight
+ * gradients).  A CTA pair computes either 256 x 256 output tiles (two
+ * accumulators in tensor memory: a tile's epilogue runs under the next
+ * tile's MMAs) or 256 x 512 tiles (one accumulator in two halves, K steps in
+ * three phases so each half drains under MMAs on the other), which move a
+ * quarter fewer operand bytes from L2 per FLOP.  mode 0 (default) always 256,
+ * 1 picks 512 where its tiles fill the GPU's waves at least as well as
+ * 256-wide ones, 2 always 512.  0, 1 or 2, else TPMLP_ERR_INVALID_ARG.  Half 0
+ * of a wide tile sums K in the narrow tile's order (bitwise equal columns);
+ * half 1 starts its sum further along K (equal within rounding).  Affects
+ * launches enqueued after the call. */
+tpmlp_status tpmlp_set_wide_tiles(int mode);
+
 /* TMA tensor-map cache.  Every call encodes one tensor map per operand shard,
  * token chunk and output of each GEMM it launches; the library keeps the
  * encoded maps in a cache keyed by every argument of the encoding (base

@@ -40,6 +40,7 @@ EXPORTED = (
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
     "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
     "tpmlp_set_head_prefetch", "tpmlp_map_cache_stats", "tpmlp_selftest_map_cache",
+    "tpmlp_set_wide_tiles",
 )
 
 
@@ -247,6 +248,12 @@ def tpmlp_set_split_min_kblocks(kblocks: int) -> None:
 
 def tpmlp_set_head_prefetch(kblocks: int) -> None:
     _check(_lib.tpmlp_set_head_prefetch(int(kblocks)), "tpmlp_set_head_prefetch")
+
+
+def tpmlp_set_wide_tiles(mode: int) -> None:
+    """0 (default): 256-wide GEMM tiles; 1: 512-wide where they fill the waves as
+    well; 2: 512-wide wherever allowed."""
+    _check(_lib.tpmlp_set_wide_tiles(int(mode)), "tpmlp_set_wide_tiles")
 
 
 def tpmlp_map_cache_stats() -> dict:

@@ -36,8 +36,12 @@ tpmlp_status device_info(DeviceInfo** out);
 //   output [rows, cols], bf16 or fp32: box 32 x 32 for the epilogue's stores
 bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, int box_rows);
 // MN-major maps are 3-D {64, K, rows / 64} when rows is a multiple of 64 (one
-// copy per box), else 2-D; *mn3d (the operand's GemmParams flag) says which.
-bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d);
+// copy per box of box_rows rows), else 2-D; *mn3d (the operand's GemmParams
+// flag) says which.
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d,
+                    int box_rows = BM);
+// Both tile widths stage B in boxes of B_ROWS rows (a wide tile's two halves
+// are two such boxes), so the operand maps do not depend on the tile width.
 bool encode_out(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, bool f32);
 
 // ---- workspace pieces ------------------------------------------------------------------
@@ -73,6 +77,10 @@ tpmlp_status check_ptr(const void* p);
 // K segments, with the device's error word and the current wait limit.
 void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int groups,
                  int ksegs);
+// Chooses the tile width of a GEMM with a bf16 output (wide tiles where they
+// fill the GPU's waves as well as narrow ones; see tpmlp_set_wide_tiles) and
+// sets tn, ntiles and total_tiles.  The B maps are encoded after this.
+void choose_tile_width(GemmParams& p, const DeviceInfo& dev);
 // Points the tail split at its workspace buffers (split_part_bytes() and
 // split_cnt_bytes() long).
 bool attach_split(GemmParams& p, void* split_part, void* split_cnt);

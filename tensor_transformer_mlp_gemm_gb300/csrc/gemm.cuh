@@ -27,7 +27,9 @@
 // of A and its own 128 rows of B per K step (32 KB), so a 6-deep ring fits in
 // shared memory and each SM keeps 192 KB of operands in flight while needing
 // only 64 B per clock at full MMA rate (a single-CTA 128 x 256 tile needs 96).
-// The pair's accumulator rows live in each CTA's own tensor memory.
+// The pair's accumulator rows live in each CTA's own tensor memory.  A
+// wider variant (256 x 512 tiles, one accumulator in two halves, see Tile)
+// moves a quarter fewer operand bytes per FLOP; the host picks the width.
 //
 // CTA layout (192 threads, persistent over tiles; both CTAs of the pair):
 //   warp 0      TMA producer (one elected thread): this CTA's A and B halves
@@ -40,7 +42,7 @@
 //               elementwise work, TMA stores; then they release the
 //               accumulator on the even CTA's "accumulator empty" barrier
 // Two 256-column fp32 accumulators in TMEM let the epilogue of one tile run
-// under the main loop of the next.
+// under the main loop of the next (256-wide tiles).
 //
 // Every mbarrier wait is bounded (GemmParams::timeout_ns).  A wait that
 // expires sets a CTA-wide abort flag and a bit of the device error word;
@@ -144,6 +146,7 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const 
 // runs fastest, so the CTAs that run at the same time share their B tiles
 // (and, across the band, their A panels) through L2.  (group, n-tile) pairs
 // form one combined N axis.
+template <int TN>
 __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& g, int& m0,
                                             int& n0) {
     const int nt_total = p.ntiles * p.groups;
@@ -155,7 +158,7 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int tile, int& 
     const int mt = mt_first + r % rows_here;
     const int ntg = r / rows_here;
     g = ntg / p.ntiles;
-    n0 = (ntg - g * p.ntiles) * BN;
+    n0 = (ntg - g * p.ntiles) * TN;
     m0 = mt * CLUSTER_M;
 }
 
@@ -415,25 +418,59 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
 
 // ---- the kernel ---------------------------------------------------------------------
 
-template <bool A_MN, bool B_MN, int EPI>
+// Tile shapes.  A pair computes a CLUSTER_M x TN output tile, TN = 256 (two
+// 256-column accumulators in TMEM, so a tile's epilogue runs under the next
+// tile's MMAs) or TN = 512 (one 512-column accumulator of two 256-column
+// halves; a K step that feeds both halves moves 48 KB per CTA for twice the
+// FLOPs of a 32 KB narrow step, a quarter fewer operand bytes per FLOP).
+//
+// A wide tile overlaps its epilogue with MMAs by splitting its K steps
+// [kbeg, kend) into three phases, L = wide_lookahead(kend - kbeg):
+//   A  steps kbeg .. kbeg+L-1   half 0 only   (stage: A + B half 0)
+//   B  steps kbeg+L .. kend-1   both halves   (stage: A + both B halves)
+//   C  steps kbeg .. kbeg+L-1   half 1 only   (stage: A again + B half 1)
+// Half 0 is complete after phase B and is drained under phase C; half 1 is
+// complete after phase C and is drained under the next tile's phase A.  Half
+// 1 sums its K steps starting at kbeg+L (a rotation of the narrow order).
+template <int TN>
+struct Tile {
+    static_assert(TN == 256 || TN == 512, "tile width 256 or 512");
+    static constexpr int kStages = TN == 512 ? 4 : STAGES;
+    static constexpr int kStageBytes = A_STAGE_BYTES + (TN / 256) * B_STAGE_BYTES;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + EPI_STAGE_BYTES + BAR_BYTES;
+    static constexpr int kChunks = TN / EPI_CHUNK;  // epilogue chunks per tile
+    static constexpr int kHalves = TN / 256;        // 256-column MMA halves
+};
+static_assert(Tile<512>::kSmemBytes <= 232448, "the wide tile's shared memory fits a CTA");
+
+// K steps of a wide tile's phases A and C (none for a one-step tile).
+constexpr int WIDE_LOOKAHEAD = 32;
+__device__ __forceinline__ int wide_lookahead(int nks) {
+    return min(WIDE_LOOKAHEAD, nks / 2);
+}
+
+template <bool A_MN, bool B_MN, int EPI, int TN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     tpmlp_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using TL = Tile<TN>;
+    constexpr int NST = TL::kStages;
+    constexpr int SB = TL::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t* epi_area = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
+    uint8_t* epi_area = smem_raw + (base - raw) + NST * SB;
     uint8_t* bar_area = epi_area + EPI_STAGE_BYTES;
-    const uint32_t epi0 = base + STAGES * STAGE_BYTES;
+    const uint32_t epi0 = base + NST * SB;
     const uint32_t bar0 = epi0 + EPI_STAGE_BYTES;
-    const uint32_t bar_full = bar0;                      // [STAGES] used in the even CTA
-    const uint32_t bar_empty = bar0 + 8 * STAGES;        // [STAGES] both CTAs
-    const uint32_t bar_tfull = bar0 + 16 * STAGES;       // [2] both CTAs
+    const uint32_t bar_full = bar0;                      // [NST] used in the even CTA
+    const uint32_t bar_empty = bar0 + 8 * NST;           // [NST] both CTAs
+    const uint32_t bar_tfull = bar0 + 16 * NST;          // [2] both CTAs
     const uint32_t bar_tempty = bar_tfull + 16;          // [2] used in the even CTA
     const uint32_t bar_drain = bar_tempty + 16;          // [1] even CTA
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 16 * STAGES + 40);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 44);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 48);
-    volatile int* epi_fail = reinterpret_cast<volatile int*>(bar_area + 16 * STAGES + 52);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 16 * NST + 40);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 16 * NST + 44);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(bar_area + 16 * NST + 48);
+    volatile int* epi_fail = reinterpret_cast<volatile int*>(bar_area + 16 * NST + 52);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -442,10 +479,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int nclusters = gridDim.x / 2;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
             ptx::mbar_init(bar_empty + 8 * s, 1);
         }
+        // TN = 256: accumulator a full / empty.  TN = 512: tfull[0] = the
+        // accumulator full, tempty[h] = its half h drained.
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar_tfull + 8 * a, 1);
             ptx::mbar_init(bar_tempty + 8 * a, 2 * EPI_WARPS * 32);  // both CTAs' epilogues
@@ -501,8 +540,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         ptx::griddep_launch_dependents();
                 }
                 int g, m0, n0;
-                decode_tile(p, it.tile, g, m0, n0);
+                decode_tile<TN>(p, it.tile, g, m0, n0);
                 const int a_row = m0 + rank * BM;
+                // B rows of half h staged by this CTA: n0 + 256 h + 128 rank
                 const int b_row = n0 + rank * B_ROWS;
                 // segment and K step advance by increments; the map and row of each
                 // operand change only with the segment
@@ -512,6 +552,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                                                   g, seg, a_row, p.K, p.a_mn3d);
                 OperandCursor cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps,
                                                   g, seg, b_row, p.K, p.b_mn3d);
+                OperandCursor cb1 = cb;
+                if (TN == 512)
+                    cb1 = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g, seg,
+                                         b_row + 256, p.K, p.b_mn3d);
                 // head prefetch: the first K steps of this pair's next tile go to L2
                 // now, a whole tile ahead of their loads (short-K GEMMs, where
                 // every tile start would otherwise wait for first-touch data)
@@ -519,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     WorkItem nx;
                     if (work_item(p, cluster, nclusters, j + 1, nk, nx)) {
                         int ng, nm0, nn0;
-                        decode_tile(p, nx.tile, ng, nm0, nn0);
+                        decode_tile<TN>(p, nx.tile, ng, nm0, nn0);
                         const int nseg = nx.kbeg / kblocks;
                         const int nkb = nx.kbeg - nseg * kblocks;
                         const OperandCursor pa =
@@ -535,15 +579,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         }
                     }
                 }
-                for (int kk = it.kbeg; kk < it.kend; ++kk) {
-                    if (kb == kblocks) {
+                const int nks = it.kend - it.kbeg;
+                const int la = TN == 512 ? wide_lookahead(nks) : 0;
+                for (int st = 0; st < nks + la; ++st) {
+                    if (TN == 512 && st == nks) {
+                        // phase C: back to the first K step of the item
+                        seg = it.kbeg / kblocks;
+                        kb = it.kbeg - seg * kblocks;
+                        ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps, g,
+                                            seg, a_row, p.K, p.a_mn3d);
+                        cb1 = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g,
+                                             seg, b_row + 256, p.K, p.b_mn3d);
+                    } else if (kb == kblocks) {
                         kb = 0;
                         ++seg;
                         ca = operand_cursor(p.a_map, p.a_part, p.a_rows_per_map, p.a_nmaps, g,
                                             seg, a_row, p.K, p.a_mn3d);
                         cb = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g,
                                             seg, b_row, p.K, p.b_mn3d);
+                        if (TN == 512)
+                            cb1 = operand_cursor(p.b_map, p.b_part, p.b_rows_per_map, p.b_nmaps, g,
+                                                 seg, b_row + 256, p.K, p.b_mn3d);
                     }
+                    // halves this step feeds: bit 0 = half 0, bit 1 = half 1
+                    const int hmask = TN == 256 ? 1 : (st < la ? 1 : (st < nks ? 3 : 2));
                     {
                         if (!wait_bounded(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p,
                                           ERR_PRODUCER)) {
@@ -552,14 +611,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         }
                         if (!p.stall_producer) {
                             const uint32_t full = even_full + 8 * stage;
-                            const uint32_t sa = base + stage * STAGE_BYTES;
+                            const uint32_t sa = base + stage * SB;
+                            const uint32_t bytes =
+                                A_STAGE_BYTES + (hmask == 3 ? 2 : 1) * B_STAGE_BYTES;
                             if (rank == 0)  // counts both CTAs' bytes
-                                ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * STAGE_BYTES);
+                                ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, 2 * bytes);
                             load_operand<A_MN, BM>(ca, kb * BK, sa, full);
-                            load_operand<B_MN, B_ROWS>(cb, kb * BK, sa + A_STAGE_BYTES, full);
+                            if (hmask & 1)
+                                load_operand<B_MN, B_ROWS>(cb, kb * BK, sa + A_STAGE_BYTES, full);
+                            if (hmask & 2)
+                                load_operand<B_MN, B_ROWS>(
+                                    cb1, kb * BK, sa + A_STAGE_BYTES + B_STAGE_BYTES, full);
                             ++fills;
                         }
-                        if (++stage == STAGES) {
+                        if (++stage == NST) {
                             stage = 0;
                             phase ^= 1u;
                         }
@@ -572,19 +637,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 // asynchronous arrive on both CTAs' "empty" barriers.  Wait until
                 // every stage filled here has been released, so no such arrive
                 // can land after this CTA has exited.
-                for (int i = 0; i < STAGES; ++i) {
+                for (int i = 0; i < NST; ++i) {
                     if (!wait_drain(bar_empty + 8 * stage, phase ^ 1u, p)) break;
-                    if (++stage == STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             } else if (rank == 0) {
-                // Wait for the pair's copies still in flight (the last STAGES
+                // Wait for the pair's copies still in flight (the last NST
                 // fills, counted on this CTA's barriers) before leaving.
-                for (long long f = (fills > STAGES ? fills - STAGES : 0); f < fills; ++f) {
-                    const int st = static_cast<int>(f % STAGES);
-                    const uint32_t par = static_cast<uint32_t>((f / STAGES) & 1);
+                for (long long f = (fills > NST ? fills - NST : 0); f < fills; ++f) {
+                    const int st = static_cast<int>(f % NST);
+                    const uint32_t par = static_cast<uint32_t>((f / NST) & 1);
                     if (!wait_drain(bar_full + 8 * st, par, p)) break;
                 }
             }
@@ -592,45 +657,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer (even CTA) ----------------
-            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(CLUSTER_M, BN, A_MN, B_MN);
+            constexpr uint32_t IDESC = ptx::idesc_bf16_f32(CLUSTER_M, 256, A_MN, B_MN);
+            constexpr uint32_t B_HALF_BYTES = 128 * BK * 2;  // half h of a CTA's B tile
             int stage = 0;
             uint32_t phase = 0;
             int lt = 0;
             bool ok = true;
+            // the MMAs of N-half h of one stage (h = 0 for TN = 256)
+            auto issue = [&](int h, uint32_t d_tmem, bool first) {
+                const uint32_t sa = base + stage * SB;
+                const uint32_t sb = sa + A_STAGE_BYTES + h * B_HALF_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    ptx::mma_bf16_pair(d_tmem + h * 256, operand_desc<A_MN>(sa, k),
+                                       operand_desc<B_MN>(sb, k), IDESC,
+                                       (!first || k > 0) ? 1u : 0u);
+                }
+            };
+            auto advance = [&]() {
+                if (++stage == NST) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
             WorkItem it;
             for (int j = 0; ok && work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
-                const int acc = lt & 1;
-                const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
-                if (!wait_bounded_cluster(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p,
-                                          ERR_MMA)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * BN);
-                for (int kk = it.kbeg; kk < it.kend; ++kk) {
-                    if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p, ERR_MMA)) {
+                if constexpr (TN == 256) {
+                    const int acc = lt & 1;
+                    const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
+                    if (!wait_bounded_cluster(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag,
+                                              p, ERR_MMA)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = base + stage * STAGE_BYTES;
-                    const uint32_t sb = sa + A_STAGE_BYTES;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        ptx::mma_bf16_pair(d_tmem, operand_desc<A_MN>(sa, k),
-                                           operand_desc<B_MN>(sb, k), IDESC,
-                                           (kk > it.kbeg || k > 0) ? 1u : 0u);
+                    const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * 256);
+                    for (int kk = it.kbeg; kk < it.kend; ++kk) {
+                        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p, ERR_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        issue(0, d_tmem, kk == it.kbeg);
+                        // the stage is free again in both CTAs of the pair
+                        ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
+                        advance();
                     }
-                    // the stage is free again in both CTAs of the pair
-                    ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    if (ok) ptx::mma_commit_pair_multicast(bar_tfull + 8 * acc, 0x3);
+                } else {
+                    // One accumulator in two halves, K steps in phases A, B, C
+                    const uint32_t ph = static_cast<uint32_t>(lt & 1);
+                    const int nks = it.kend - it.kbeg;
+                    const int la = wide_lookahead(nks);
+                    for (int st = 0; st < nks + la; ++st) {
+                        // half 0 (phase A) needs the previous tile's half 0
+                        // drained, half 1 (phase B on) its half 1
+                        if (st == 0 &&
+                            !wait_bounded_cluster(bar_tempty, ph ^ 1u, abort_flag, p, ERR_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        if (st == la && !wait_bounded_cluster(bar_tempty + 8, ph ^ 1u, abort_flag,
+                                                              p, ERR_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!wait_bounded(bar_full + 8 * stage, phase, abort_flag, p, ERR_MMA)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        if (st < nks) issue(0, tmem, st == 0);
+                        if (st >= la) issue(1, tmem, st == la);
+                        ptx::mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
+                        // half 0 complete after phase B, half 1 after phase C
+                        if (st == nks - 1) ptx::mma_commit_pair_multicast(bar_tfull, 0x3);
+                        if (st == nks + la - 1) ptx::mma_commit_pair_multicast(bar_tfull + 8, 0x3);
+                        advance();
                     }
                 }
-                if (ok)
-                    ptx::mma_commit_pair_multicast(bar_tfull + 8 * acc, 0x3);
             }
             // Every MMA this thread issued must finish before TMEM is freed.
             ptx::mma_commit_pair(bar_drain);
@@ -638,10 +743,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // MMA tail: both CTAs' epilogues release the last accumulators with
             // arrives on this CTA's barriers; wait for them before leaving.
             if (ok) {
-                for (int j = (lt > 2 ? lt - 2 : 0); j < lt; ++j) {
-                    if (!wait_drain(bar_tempty + 8 * (j & 1),
-                                    static_cast<uint32_t>((j >> 1) & 1), p))
-                        break;
+                if constexpr (TN == 256) {
+                    for (int j = (lt > 2 ? lt - 2 : 0); j < lt; ++j) {
+                        if (!wait_drain(bar_tempty + 8 * (j & 1),
+                                        static_cast<uint32_t>((j >> 1) & 1), p))
+                            break;
+                    }
+                } else if (lt > 0) {
+                    const uint32_t par = static_cast<uint32_t>((lt - 1) & 1);
+                    if (wait_drain(bar_tempty, par, p)) wait_drain(bar_tempty + 8, par, p);
                 }
             }
         }
@@ -678,6 +788,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 ptx::bulk_commit_group();
             }
         };
+        // Releases accumulator part `a` (TN = 256: accumulator a; TN = 512:
+        // half a) once this warp's loads from it have completed.
+        auto release = [&](int a) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive_cluster(even_tempty + 8 * a);
+        };
 
         // fp32 outputs (the weight gradients: short K, 128 KB per CTA per tile)
         // are stored paced over most of the time the next tile's MMAs take:
@@ -690,10 +806,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         WorkItem it;
         for (int j = 0; work_item(p, cluster, nclusters, j, nk, it); ++j, ++lt) {
             int g, mp, n0;
-            decode_tile(p, it.tile, g, mp, n0);
+            decode_tile<TN>(p, it.tile, g, mp, n0);
             const int m0 = mp + rank * BM;  // this CTA's first row
-            const int acc = lt & 1;
-            const uint32_t acc_phase = static_cast<uint32_t>((lt >> 1) & 1);
+            const int acc = TN == 256 ? (lt & 1) : 0;
+            const uint32_t acc_phase =
+                static_cast<uint32_t>(TN == 256 ? ((lt >> 1) & 1) : (lt & 1));
             // output map and row coordinate of this warp's 32 rows
             int part = g;
             int y0 = m0 + quarter * 32;
@@ -707,16 +824,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             uint4 pre[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                             make_uint4(0, 0, 0, 0)};
             if (it.unit < 0) load_in0<EPI>(p, part, in_row, m, n0, pre);
-            const bool ok = wait_bounded(bar_tfull + 8 * acc, acc_phase, abort_flag, p,
-                                         ERR_EPILOGUE);
-            // all four epilogue warps give up together (they share named barriers)
-            if (!ok) *epi_fail = 1;
-            epilogue_bar();
-            if (*epi_fail) break;
-            __syncwarp();
-            ptx::tc_fence_after();
+            // Waits for accumulator part b (TN = 256: accumulator b; TN = 512:
+            // half b); all four epilogue warps give up together (they share
+            // named barriers).
+            auto acc_ready = [&](int b) -> bool {
+                const bool ok = wait_bounded(bar_tfull + 8 * b, acc_phase, abort_flag, p,
+                                             ERR_EPILOGUE);
+                if (!ok) *epi_fail = 1;
+                epilogue_bar();
+                if (*epi_fail) return false;
+                __syncwarp();
+                ptx::tc_fence_after();
+                return true;
+            };
+            if (!acc_ready(acc)) break;
             long long pace_t0 = 0, pace_clk = 0;
-            if constexpr (EPI == EPI_F32) {
+            if constexpr (EPI == EPI_F32 && TN == 256) {
                 // only while this pair has a next tile whose main loop the stores can
                 // hide under; the last tile's stores go out at once
                 WorkItem nx;
@@ -726,21 +849,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc * BN);
+                                   static_cast<uint32_t>(acc * 256);
             const CUtensorMap* out1 = &p.out_map[part];
             const CUtensorMap* out2 = (EPI == EPI_BIAS_GELU || EPI == EPI_DGELU_H)
                                           ? &p.out_map[MAX_MAPS + part]
                                           : nullptr;
             constexpr bool OUT_F32 = EPI == EPI_F32;
+            constexpr int NCH = TL::kChunks;
 
             if (it.unit < 0) {
                 // whole tile: fused epilogue straight from the accumulator
+                bool failed = false;
 #pragma unroll 1
-                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                for (int c = 0; c < NCH; ++c) {
+                    if (TN == 512 && c == NCH / 2) {
+                        release(0);  // half 0 drained
+                        if (!acc_ready(1)) {
+                            failed = true;
+                            break;
+                        }
+                    }
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                     uint4 cur[4] = {pre[0], pre[1], pre[2], pre[3]};
-                    if (c + 1 < BN / EPI_CHUNK)  // next chunk's second input, in flight meanwhile
+                    if (c + 1 < NCH)  // next chunk's second input, in flight meanwhile
                         load_in0<EPI>(p, part, in_row, m, n0 + (c + 1) * EPI_CHUNK, pre);
                     ptx::tmem_ld_wait();
                     const int n = n0 + c * EPI_CHUNK;
@@ -752,15 +884,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     if (pace_clk && c > 0) pace_until(pace_t0 + c * pace_clk);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                 }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive_cluster(even_tempty + 8 * acc);
+                if (failed) break;
+                release(TN == 256 ? acc : 1);
                 continue;
             }
 
-            // split unit: store this unit's raw partial rows, then count it
-            const int prow = (it.unit * 2 + rank) * BM + quarter * 32;
+            // split unit: store this unit's raw partial rows, then count it.
+            // Partial row block v = unit * halves + h holds N-half h of the unit.
+            bool failed = false;
 #pragma unroll 1
-            for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+            for (int c = 0; c < NCH; ++c) {
+                if (TN == 512 && c == NCH / 2) {
+                    release(0);
+                    if (!acc_ready(1)) {
+                        failed = true;
+                        break;
+                    }
+                }
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                 ptx::tmem_ld_wait();
@@ -769,10 +909,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 float x[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
-                store_box(&p.part_map, nullptr, c * EPI_CHUNK, prow, x, x, true);
+                const int vblk = it.unit * TL::kHalves + (c >> 3);
+                const int prow = (vblk * 2 + rank) * BM + quarter * 32;
+                store_box(&p.part_map, nullptr, (c & 7) * EPI_CHUNK, prow, x, x, true);
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive_cluster(even_tempty + 8 * acc);
+            if (failed) break;
+            release(TN == 256 ? acc : 1);
             // the partial is complete and visible before it is counted
             if (lane == 0) {
                 ptx::bulk_wait_group<0>();
@@ -793,23 +935,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 __threadfence();
                 const int u0 = (it.tile - p.dp_tiles) * p.splits;
 #pragma unroll 1
-                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                for (int c = 0; c < NCH; ++c) {
                     const int n = n0 + c * EPI_CHUNK;
                     if (n >= p.N || m0 >= p.M) continue;
                     float x[32], x2[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = 0.f;
-                    for (int sp = 0; sp < p.splits; ++sp) {
-                        const long long r = static_cast<long long>((u0 + sp) * 2 + rank) * BM + row;
-                        const float4* src =
-                            reinterpret_cast<const float4*>(p.partial + r * BN + c * EPI_CHUNK);
+                    // four units' rows in flight per round (the loads are
+                    // independent), added in unit order
+                    for (int sp0 = 0; sp0 < p.splits; sp0 += 4) {
+                        float4 f[4][8];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 f = __ldcg(src + q);
-                            x[4 * q] += f.x;
-                            x[4 * q + 1] += f.y;
-                            x[4 * q + 2] += f.z;
-                            x[4 * q + 3] += f.w;
+                        for (int u = 0; u < 4; ++u) {
+                            if (sp0 + u < p.splits) {
+                                const int vblk = (u0 + sp0 + u) * TL::kHalves + (c >> 3);
+                                const long long r =
+                                    static_cast<long long>(vblk * 2 + rank) * BM + row;
+                                const float4* src = reinterpret_cast<const float4*>(
+                                    p.partial + r * BN + (c & 7) * EPI_CHUNK);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) f[u][q] = __ldcg(src + q);
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (sp0 + u < p.splits) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    x[4 * q] += f[u][q].x;
+                                    x[4 * q + 1] += f[u][q].y;
+                                    x[4 * q + 2] += f[u][q].z;
+                                    x[4 * q + 3] += f[u][q].w;
+                                }
+                            }
                         }
                     }
                     uint4 in[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
@@ -840,18 +998,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
 // CTA pairs of this kernel variant that fit on the GPU at once (queried once
 // per variant).
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, int TN>
 cudaError_t max_active_clusters(int& out) {
     static int max_clusters = 0;
     if (max_clusters == 0) {
-        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI>;
+        auto kern = tpmlp_gemm_kernel<A_MN, B_MN, EPI, TN>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             GEMM_SMEM_BYTES);
+                                             Tile<TN>::kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+        cfg.dynamicSmemBytes = Tile<TN>::kSmemBytes;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
         attr.val.clusterDim.x = 2;
@@ -870,33 +1028,35 @@ cudaError_t max_active_clusters(int& out) {
 }
 
 // Launched as a programmatic dependent of the previous kernel in the stream.
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, int TN>
 cudaError_t launch_variant(const GemmParams& p, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.dynamicSmemBytes = Tile<TN>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tpmlp_gemm_kernel<A_MN, B_MN, EPI>, p);
+    return cudaLaunchKernelEx(&cfg, tpmlp_gemm_kernel<A_MN, B_MN, EPI, TN>, p);
 }
 
 // Persistent launch, capped at the pairs that fit on the GPU at once; the
 // tiles of an incomplete last wave get their K range split across the pairs
-// that would otherwise idle.
-template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
+// that would otherwise idle.  A wide tile's split unit takes two partial-tile
+// slots of the workspace (one per N-half).
+template <bool A_MN, bool B_MN, int EPI, int TN>
+cudaError_t launch_tiles(const GemmParams& p_in, cudaStream_t stream) {
     GemmParams p = p_in;
     int P = 0;
-    cudaError_t e = max_active_clusters<A_MN, B_MN, EPI>(P);
+    cudaError_t e = max_active_clusters<A_MN, B_MN, EPI, TN>(P);
     if (e != cudaSuccess) return e;
     const int nk = ((p.K + BK - 1) / BK) * p.ksegs;
     const int full = p.total_tiles / P;
     const int left = p.total_tiles % P;
+    constexpr int max_units = MAX_SPLIT_UNITS / Tile<TN>::kHalves;
     p.dp_tiles = p.total_tiles;
     p.units = 0;
     p.splits = 1;
@@ -904,7 +1064,7 @@ cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
         int splits = P / left;
         if (splits > MAX_SPLITS) splits = MAX_SPLITS;
         if (splits > nk) splits = nk;
-        if (splits >= 2 && left * splits <= MAX_SPLIT_UNITS) {
+        if (splits >= 2 && left * splits <= max_units) {
             p.splits = splits;
             p.units = left * splits;
             p.dp_tiles = p.total_tiles - left;
@@ -916,7 +1076,18 @@ cudaError_t launch_clusters(const GemmParams& p_in, cudaStream_t stream) {
         e = cudaMemsetAsync(p.counters, 0, sizeof(int) * 2 * left, stream);
         if (e != cudaSuccess) return e;
     }
-    return launch_variant<A_MN, B_MN, EPI>(p, clusters, stream);
+    return launch_variant<A_MN, B_MN, EPI, TN>(p, clusters, stream);
+}
+
+// The tile width the host chose (GemmParams::tn); fp32-output GEMMs (the
+// weight gradients, short K and a large epilogue) always run narrow tiles.
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_clusters(const GemmParams& p, cudaStream_t stream) {
+    if constexpr (EPI != EPI_F32) {
+        if (p.tn == 512) return launch_tiles<A_MN, B_MN, EPI, 512>(p, stream);
+    }
+    if (p.tn != 256) return cudaErrorInvalidValue;
+    return launch_tiles<A_MN, B_MN, EPI, 256>(p, stream);
 }
 
 #define TPMLP_GEMM_LAUNCHER(NAME, A_MN, B_MN, EPI)               \

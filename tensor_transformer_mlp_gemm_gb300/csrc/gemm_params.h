@@ -11,12 +11,14 @@
 
 namespace tpmlp {
 
-// A CTA pair (cluster of 2) computes a CLUSTER_M x BN tile with
+// A CTA pair (cluster of 2) computes a CLUSTER_M x TN tile with
 // tcgen05.mma.cta_group::2: each CTA stages its own BM rows of A and its own
-// BN/2 rows of B per K step and holds BM rows x BN columns of the accumulator.
+// TN/2 rows of B per K step and holds BM rows x TN columns of the accumulator.
+// TN is BN (narrow tiles, two accumulators) or BN_WIDE (one accumulator).
 constexpr int BM = 128;            // tile rows per CTA (TMEM lanes)
 constexpr int CLUSTER_M = 2 * BM;  // tile rows per CTA pair
-constexpr int BN = 256;       // tile columns (TMEM columns per accumulator)
+constexpr int BN = 256;       // narrow tile columns (TMEM columns per accumulator)
+constexpr int BN_WIDE = 512;  // wide tile columns (the whole of TMEM)
 constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
 constexpr int STAGES = 6;
 constexpr int A_STAGE_BYTES = BM * BK * 2;
@@ -93,7 +95,8 @@ struct GemmParams {
     CUtensorMap part_map;   // fp32 [MAX_SPLIT_UNITS * CLUSTER_M, BN] partial tiles
     const float* partial;   // same buffer, for the summing loads
     int* counters;          // [MAX_SPLIT_UNITS][2] arrivals per leftover tile and CTA
-    int mtiles, ntiles, total_tiles, band;  // cluster tiles of CLUSTER_M x BN
+    int tn;                 // tile columns: BN or BN_WIDE (set with mtiles, ntiles)
+    int mtiles, ntiles, total_tiles, band;  // pair tiles of CLUSTER_M x tn
     // epilogue: TMA store maps (box 32 x 32, 128-byte swizzle for fp32,
     // 64-byte swizzle for bf16) and the saved pre-activation for EPI_DGELU
     CUtensorMap out_map[2 * MAX_MAPS];

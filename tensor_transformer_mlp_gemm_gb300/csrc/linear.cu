@@ -128,13 +128,15 @@ tpmlp_status column_forward(const Lin& s, const DeviceInfo* dev, const void* con
     // Y_i = X.W_i + b_i: t groups, M = T, N = oi, K = in
     GemmParams p;
     base_params(p, *dev, s.T, s.shard, s.in, s.t, 1);
+    choose_tile_width(p, *dev);
     for (int j = 0; j < s.chunks; ++j)
         if (!encode_kmajor(&p.a_map[j], X[j], s.in, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
     p.a_part = PART_ROW;
     p.a_nmaps = s.chunks;
     p.a_rows_per_map = s.Tc;
     for (int i = 0; i < s.t; ++i)
-        if (!encode_mnmajor(&p.b_map[i], W[i], s.shard, s.in, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
+        if (!encode_mnmajor(&p.b_map[i], W[i], s.shard, s.in, &p.b_mn3d))
+            return TPMLP_ERR_UNSUPPORTED;
     p.b_part = PART_GROUP;
     p.b_nmaps = s.t;
     for (int i = 0; i < s.t; ++i)
@@ -154,9 +156,10 @@ tpmlp_status column_backward(const Lin& s, const DeviceInfo* dev, const void* co
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.in, s.shard, 1, s.t);
+        choose_tile_width(p, *dev);
         for (int i = 0; i < s.t; ++i) {
             if (!encode_kmajor(&p.a_map[i], dY[i], s.shard, s.T, BM)) return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_kmajor(&p.b_map[i], W[i], s.shard, s.in, BN / 2))
+            if (!encode_kmajor(&p.b_map[i], W[i], s.shard, s.in, B_ROWS))
                 return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = p.b_part = PART_KSEG;
@@ -198,9 +201,11 @@ tpmlp_status row_forward(const Lin& s, const DeviceInfo* dev, const void* const*
     // Z = sum_i X_i.W_i + b: M = T, N = out, K = ii per segment; rows into chunks
     GemmParams p;
     base_params(p, *dev, s.T, s.out, s.shard, 1, s.t);
+    choose_tile_width(p, *dev);
     for (int i = 0; i < s.t; ++i) {
         if (!encode_kmajor(&p.a_map[i], X[i], s.shard, s.T, BM)) return TPMLP_ERR_UNSUPPORTED;
-        if (!encode_mnmajor(&p.b_map[i], W[i], s.out, s.shard, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
+        if (!encode_mnmajor(&p.b_map[i], W[i], s.out, s.shard, &p.b_mn3d))
+            return TPMLP_ERR_UNSUPPORTED;
     }
     p.a_part = p.b_part = PART_KSEG;
     p.a_nmaps = p.b_nmaps = s.t;
@@ -221,13 +226,14 @@ tpmlp_status row_backward(const Lin& s, const DeviceInfo* dev, const void* const
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.shard, s.out, s.t, 1);
+        choose_tile_width(p, *dev);
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_kmajor(&p.a_map[j], dZ[j], s.out, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_ROW;
         p.a_nmaps = s.chunks;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_kmajor(&p.b_map[i], W[i], s.out, s.shard, BN / 2))
+            if (!encode_kmajor(&p.b_map[i], W[i], s.out, s.shard, B_ROWS))
                 return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_nmaps = s.t;

@@ -55,6 +55,7 @@ DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = 2000000000ULL;
 int g_split_min_kblocks = DEFAULT_SPLIT_MIN_KBLOCKS;
 int g_head_prefetch = 0;
+int g_wide_tiles = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -145,10 +146,10 @@ bool encode_kmajor(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, i
     return encode_bf16(m, ptr, K, rows, K, BK, static_cast<uint32_t>(box_rows));
 }
 
-static_assert(BM == B_ROWS, "one 3-D MN-major box height serves both operands");
-
-bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d) {
-    if (rows % MN_CHUNK != 0) {
+bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, int* mn3d,
+                    int box_rows) {
+    if (rows % MN_CHUNK != 0 || rows < static_cast<uint64_t>(box_rows)) {
+        // 2-D map {rows, K}: a box is fetched as box_rows / 64 copies of {64, BK}
         *mn3d = 0;
         return encode_bf16(m, ptr, rows, K, rows, MN_CHUNK, BK);
     }
@@ -157,7 +158,7 @@ bool encode_mnmajor(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, 
     *mn3d = 1;
     cuuint64_t dims[3] = {MN_CHUNK, K, rows / MN_CHUNK};
     cuuint64_t strides[2] = {rows * 2, MN_CHUNK * 2};
-    cuuint32_t box[3] = {MN_CHUNK, BK, static_cast<cuuint32_t>(BM / MN_CHUNK)};
+    cuuint32_t box[3] = {MN_CHUNK, BK, static_cast<cuuint32_t>(box_rows / MN_CHUNK)};
     return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
@@ -200,6 +201,7 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     p.K = K;
     p.groups = groups;
     p.ksegs = ksegs;
+    p.tn = BN;
     p.mtiles = (M + CLUSTER_M - 1) / CLUSTER_M;
     p.ntiles = (N + BN - 1) / BN;
     p.total_tiles = p.mtiles * p.ntiles * groups;
@@ -211,6 +213,38 @@ void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int 
     p.bias_group_stride = 0;
     p.ld_in = 0;
     for (int i = 0; i < MAX_MAPS; ++i) p.in0[i] = nullptr;
+}
+
+// Waves of pair tiles a GEMM takes at tile width tn on `pairs` pairs, with the
+// tail split's division of an incomplete last wave (as the launcher applies it).
+static double tile_waves(const GemmParams& p, int tn, int pairs) {
+    const long long ntiles = (p.N + tn - 1) / tn;
+    const long long tiles = static_cast<long long>(p.mtiles) * ntiles * p.groups;
+    const long long full = tiles / pairs, left = tiles % pairs;
+    if (left == 0) return static_cast<double>(full);
+    const int nk = ((p.K + BK - 1) / BK) * p.ksegs;
+    long long splits = pairs / left;
+    if (splits > MAX_SPLITS) splits = MAX_SPLITS;
+    if (splits > nk) splits = nk;
+    const bool split = g_split_min_kblocks > 0 && nk >= g_split_min_kblocks && splits >= 2 &&
+                       left * splits <= MAX_SPLIT_UNITS / (tn / BN);
+    return static_cast<double>(full) + (split ? 1.0 / static_cast<double>(splits) : 1.0);
+}
+
+void choose_tile_width(GemmParams& p, const DeviceInfo& dev) {
+    int tn = BN;
+    if (g_wide_tiles == 2) {
+        tn = BN_WIDE;
+    } else if (g_wide_tiles == 1) {
+        // the same work in no more time: waves x tile width (a wide tile is
+        // twice a narrow one's work); ties go to the wide tile, which moves a
+        // quarter fewer operand bytes per FLOP
+        const int pairs = dev.sm_count / 2 > 0 ? dev.sm_count / 2 : 1;
+        if (tile_waves(p, BN_WIDE, pairs) * BN_WIDE <= tile_waves(p, BN, pairs) * BN) tn = BN_WIDE;
+    }
+    p.tn = tn;
+    p.ntiles = (p.N + tn - 1) / tn;
+    p.total_tiles = p.mtiles * p.ntiles * p.groups;
 }
 
 bool attach_split(GemmParams& p, void* split_part, void* split_cnt) {
@@ -329,6 +363,7 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        choose_tile_width(p, *dev);
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_kmajor(&p.a_map[j], X[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_ROW;
@@ -336,7 +371,8 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
         p.b_nmaps = s.t;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], A_shards[i], s.fi, s.h, &p.b_mn3d))
+                return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
@@ -356,10 +392,12 @@ tpmlp_status run_forward(const Shapes& s, const DeviceInfo* dev, const void* con
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        choose_tile_width(p, *dev);
         for (int i = 0; i < s.t; ++i) {
             if (!encode_kmajor(&p.a_map[i], shard_ptr(H, i, s), s.fi, s.T, BM))
                 return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi, &p.b_mn3d)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_mnmajor(&p.b_map[i], B_shards[i], s.h, s.fi, &p.b_mn3d))
+                return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = PART_KSEG;
         p.a_nmaps = s.t;
@@ -400,6 +438,7 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.fi, s.h, s.t, 1);
+        choose_tile_width(p, *dev);
         for (int j = 0; j < s.chunks; ++j)
             if (!encode_kmajor(&p.a_map[j], dZ[j], s.h, s.Tc, BM)) return TPMLP_ERR_UNSUPPORTED;
         p.a_part = PART_ROW;
@@ -407,7 +446,8 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
         p.b_nmaps = s.t;
         p.a_rows_per_map = s.Tc;
         for (int i = 0; i < s.t; ++i)
-            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], B_shards[i], s.h, s.fi, B_ROWS))
+                return TPMLP_ERR_UNSUPPORTED;
         p.b_part = PART_GROUP;
         p.b_rows_per_map = 0;
         for (int i = 0; i < s.t; ++i) {
@@ -433,10 +473,12 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
     {
         GemmParams p;
         base_params(p, *dev, s.T, s.h, s.fi, 1, s.t);
+        choose_tile_width(p, *dev);
         for (int i = 0; i < s.t; ++i) {
             if (!encode_kmajor(&p.a_map[i], shard_ptr(dY, i, s), s.fi, s.T, BM))
                 return TPMLP_ERR_UNSUPPORTED;
-            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
+            if (!encode_kmajor(&p.b_map[i], A_shards[i], s.fi, s.h, B_ROWS))
+                return TPMLP_ERR_UNSUPPORTED;
         }
         p.a_part = PART_KSEG;
         p.a_nmaps = s.t;
@@ -573,6 +615,13 @@ TPMLP_API tpmlp_status tpmlp_set_head_prefetch(int kblocks) {
     if (kblocks < 0 || kblocks > 64) return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     g_head_prefetch = kblocks;
+    return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_set_wide_tiles(int mode) {
+    if (mode < 0 || mode > 2) return TPMLP_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_wide_tiles = mode;
     return TPMLP_OK;
 }
 
@@ -792,7 +841,7 @@ TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b,
     GemmParams p;
     base_params(p, *dev, BM, BN, BK, 1, 1);
     if (!encode_kmajor(&p.a_map[0], a, BK, BM, BM)) return TPMLP_ERR_UNSUPPORTED;
-    if (!encode_kmajor(&p.b_map[0], b, BK, BN, BN / 2)) return TPMLP_ERR_UNSUPPORTED;
+    if (!encode_kmajor(&p.b_map[0], b, BK, BN, B_ROWS)) return TPMLP_ERR_UNSUPPORTED;
     p.a_part = p.b_part = PART_SINGLE;
     p.a_rows_per_map = p.b_rows_per_map = 0;
     if (!encode_out(&p.out_map[0], c, BN, BM, false)) return TPMLP_ERR_UNSUPPORTED;

@@ -262,3 +262,21 @@ def test_rejects_bad_arguments_on_device():
     with pytest.raises(binding.TpmlpError) as e:
         binding.tpmlp_column_linear_forward(lin.dims, lin.X, lin.W, lin.b, lin.Y, off)
     assert e.value.status == binding.TPMLP_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("split", ["column", "row"])
+@pytest.mark.parametrize("T,din,dout,t,chunks", [
+    (333, 264, 1032, 3, 1),
+    (512, 1024, 2048, 4, 4),
+])
+def test_wide_tiles_full(split, T, din, dout, t, chunks):
+    """The linear layers' bf16-output GEMMs on 256 x 512 pair tiles."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    binding.tpmlp_set_wide_tiles(2)
+    try:
+        if split == "column":
+            _run_full(custom_linear(T, din, dout, t, split, sigma_w=0.05, seq_chunks=chunks), seed=5)
+        else:
+            _run_full(custom_linear(T, dout, din, t, split, sigma_w=0.05, seq_chunks=chunks), seed=5)
+    finally:
+        binding.tpmlp_set_wide_tiles(0)

@@ -276,3 +276,66 @@ def test_tensor_map_cache_hits_on_repeat_and_misses_on_new_buffers():
     s2 = binding.tpmlp_map_cache_stats()
     assert s2["misses"] > s1["misses"], "new buffers reused another buffer's maps"
     _assert_bitwise(b.Z + b.dA, first, "new buffers")
+
+
+@pytest.fixture
+def wide_tiles_forced():
+    """Run every bf16-output GEMM with 256 x 512 pair tiles, whatever the size."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    binding.tpmlp_set_wide_tiles(2)
+    yield
+    binding.tpmlp_set_wide_tiles(0)
+
+
+@pytest.mark.parametrize("T,h,f,t,chunks", [
+    (128, 256, 1024, 2, 1),     # the tiny workload
+    (333, 264, 1032, 3, 1),     # ragged M, N and K tails; wide tiles mostly past N
+    (77, 72, 272, 2, 1),        # smaller than one tile in every dimension
+    (512, 256, 1024, 4, 4),     # token chunks
+    (300, 1040, 2064, 2, 1),    # several wide tiles per row, ragged last one
+])
+def test_wide_tiles_full(wide_tiles_forced, T, h, f, t, chunks):
+    _run_full(custom(T, h, f, t, sigma_w=0.05, seq_chunks=chunks), seed=16)
+
+
+@pytest.mark.parametrize("T,h,f,t,chunks", [
+    (128, 256, 1024, 2, 1),
+    (333, 264, 1032, 3, 1),
+    (512, 256, 1024, 4, 4),
+])
+def test_wide_tiles_tail_split_full(wide_tiles_forced, forced_tail_split, T, h, f, t, chunks):
+    _run_full(custom(T, h, f, t, sigma_w=0.05, seq_chunks=chunks), seed=17)
+
+
+def test_wide_tiles_match_narrow():
+    """Without the tail split, half 0 of a wide tile sums every output in the
+    same order as a narrow tile (bitwise equal columns); half 1 starts its K
+    sum further along (within the parity gate)."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    from parity import gate
+    w = custom(600, 1040, 2064, 2, seq_chunks=1)
+    inputs = make_inputs(w, 18)
+    binding.tpmlp_set_split_min_kblocks(0)
+    try:
+        binding.tpmlp_set_wide_tiles(0)
+        narrow = _block(w, inputs)
+        narrow.step()
+        binding.tpmlp_set_wide_tiles(2)
+        wide = _block(w, inputs)
+        wide.step()
+    finally:
+        binding.tpmlp_set_wide_tiles(0)
+        binding.tpmlp_set_split_min_kblocks(128)
+    torch.cuda.synchronize()
+    sn, sw = narrow.saved(), wide.saved()
+    fi = w.ffn // w.t
+    half0 = (torch.arange(fi, device=sn["Y"][0].device) % 512) < 256
+    for k in ("Y", "H", "dY"):
+        for i in range(w.t):
+            assert torch.equal(sw[k][i][:, half0], sn[k][i][:, half0]), f"{k}[{i}] half 0"
+            gate(f"{k}[{i}] wide vs narrow", sw[k][i].cpu(), sn[k][i].cpu())
+    gate("Z wide vs narrow", wide.Z[0].cpu(), narrow.Z[0].cpu())
+    gate("dX wide vs narrow", wide.dX[0].cpu(), narrow.dX[0].cpu())
+    for i in range(w.t):
+        gate(f"dA[{i}] wide vs narrow", wide.dA[i].cpu(), narrow.dA[i].cpu())
+        gate(f"dB[{i}] wide vs narrow", wide.dB[i].cpu(), narrow.dB[i].cpu())

@@ -96,6 +96,20 @@ def test_sp_layer_full(T, h, f, t, chunks, p):
     _run_full(custom(T, h, f, t, seq_chunks=chunks), p, seed=2)
 
 
+@pytest.mark.parametrize("T,h,f,t,chunks,p", [
+    (512, 256, 1024, 4, 4, 0.1),
+    (333, 264, 1032, 3, 1, 0.2),
+])
+def test_sp_layer_wide_tiles_full(T, h, f, t, chunks, p):
+    """The dropout + residual epilogue and the rest on 256 x 512 pair tiles."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    binding.tpmlp_set_wide_tiles(2)
+    try:
+        _run_full(custom(T, h, f, t, seq_chunks=chunks), p, seed=6)
+    finally:
+        binding.tpmlp_set_wide_tiles(0)
+
+
 def test_sp_layer_deterministic_and_seeded():
     w = custom(512, 256, 1024, 4, seq_chunks=4)
     inputs = make_sp_inputs(w, 3)
