@@ -635,8 +635,10 @@ class MlpRunner:
         self.flops_step = 12.0 * T * h * f
         self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
         self.gemm_flops = 2.0 * T * h * f  # every GEMM launch
-        # column sums: read dY [T, f] and dZ [T, h] bf16, write db1, db2 fp32, per step
-        self.colsum_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
+        # bias-gradient kernels per step: db1 adds the dH GEMM's fp32 column sums
+        # of each 32-row group (read ceil(T/32) x f x 4 bytes, write f x 4); db2
+        # sums dZ (read T x h x 2, write h x 4)
+        self.colsum_bytes = ((T + 31) // 32) * f * 4 + f * 4 + T * h * 2 + h * 4
         self.l2_note = (f"inputs larger than L2 (bf16 weights {2 * h * f * 2 / 1e9:.2f} GB, "
                         f"activations {3 * T * f * 2 / 1e9:.2f} GB per step)")
         self.ins, self.outs = ("X", "dZ"), ("Z", "dX")  # per-step uploads; fwd, bwd results
@@ -696,7 +698,7 @@ class SpRunner(MlpRunner):
         self.flops_step = 12.0 * T * h * f
         self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
         self.gemm_flops = 2.0 * T * h * f
-        self.colsum_bytes = T * f * 2 + T * h * 2 + (f + h) * 4
+        self.colsum_bytes = ((T + 31) // 32) * f * 4 + f * 4 + T * h * 2 + h * 4
         # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes
         # dX (the dgamma / dbeta pass re-reads X and dLN(X): not counted, algorithmic bytes only)
         self.ln_fwd_bytes = 2 * T * h * 2

@@ -96,6 +96,49 @@ __global__ void colsum_finish_kernel(const float* __restrict__ partial, int spli
     out[o] = s;
 }
 
+// CTA = 16 column quads (64 columns) x 16 row lanes; lane r sums rows r,
+// r + 16, ... of its four columns with 16-byte loads, then the 16 lanes are
+// combined in a fixed order.
+__global__ void __launch_bounds__(256) colsum_f32_kernel(const float* __restrict__ part,
+                                                         long long rows, long long ld,
+                                                         long long ncols, float* __restrict__ out) {
+    __shared__ float4 red[16][16];
+    const int quad = threadIdx.x & 15;
+    const int lane_r = threadIdx.x >> 4;
+    const long long c = (static_cast<long long>(blockIdx.x) * 16 + quad) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < ncols) {
+        for (long long r = lane_r; r < rows; r += 16) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(part + r * ld + c));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+    }
+    red[lane_r][quad] = acc;
+    __syncthreads();
+    if (lane_r == 0 && c < ncols) {
+        float4 s = red[0][quad];
+        for (int k = 1; k < 16; ++k) {
+            const float4 v = red[k][quad];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        *reinterpret_cast<float4*>(out + c) = s;
+    }
+}
+
+cudaError_t launch_colsum_f32(const float* part, long long rows, long long ld, long long ncols,
+                              float* out, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((ncols + 63) / 64);
+    if (blocks == 0) return cudaSuccess;
+    colsum_f32_kernel<<<blocks, 256, 0, stream>>>(part, rows, ld, ncols, out);
+    return cudaGetLastError();
+}
+
 dim3 colsum_plan(ColsumParams& p, int sm_count) {
     const int strips = (p.ncols + CS_COLS - 1) / CS_COLS;
     const int groups = p.mode == CS_COLS_CONCAT ? p.nparts : 1;

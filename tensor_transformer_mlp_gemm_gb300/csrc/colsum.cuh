@@ -40,4 +40,11 @@ inline size_t colsum_scratch_bytes(long long n_out) {
 // when the rows are split).  Deterministic: no atomics.
 cudaError_t launch_colsum(const ColsumParams& p, dim3 grid, cudaStream_t stream, int* launches);
 
+// fp32 column sums of a [rows, ld] partial-sum matrix (its first ncols
+// columns): out[c] = sum over r of part[r * ld + c], r in increasing order
+// within each of 16 row lanes, the 16 lanes then added in lane order.  ncols
+// and ld multiples of 4, part and out 16-byte aligned.
+cudaError_t launch_colsum_f32(const float* part, long long rows, long long ld, long long ncols,
+                              float* out, cudaStream_t stream);
+
 }  // namespace tpmlp

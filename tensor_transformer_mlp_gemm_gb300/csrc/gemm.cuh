@@ -416,6 +416,33 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
     }
 }
 
+// Column sums of one warp's 32 x 32 block of the fp32 output (lane = row,
+// x[j] = column n + j), rows at or past M counted as zero: a butterfly of 31
+// shuffles leaves lane j with the sum of column n + j over the 32 rows, which
+// it stores into the partial row of this 32-row group (one 128-byte store per
+// warp).  The order of the additions is fixed, so the sums are reproducible.
+// Works in place: x is consumed (called after the values have been staged).
+__device__ __forceinline__ void warp_column_sums(const GemmParams& p, int g, int first_row, int m,
+                                                 int n, int lane, float (&x)[32]) {
+    if (m >= p.M) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = 0.f;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = upper ? x[i] : x[i + o];
+            const float keep = upper ? x[i + o] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    if (first_row < p.M && n + lane < p.N)
+        p.colsum_part[static_cast<long long>(first_row / 32) * p.colsum_ld +
+                      static_cast<long long>(g) * p.N + n + lane] = x[0];
+}
+
 // ---- the kernel ---------------------------------------------------------------------
 
 // Tile shapes.  A pair computes a CLUSTER_M x TN output tile, TN = 256 (two
@@ -883,6 +910,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, cur);
                     if (pace_clk && c > 0) pace_until(pace_t0 + c * pace_clk);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
+                    if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
+                        if (p.colsum_part) warp_column_sums(p, g, m0 + quarter * 32, m, n, lane, x);
+                    }
                 }
                 if (failed) break;
                 release(TN == 256 ? acc : 1);
@@ -941,12 +971,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     float x[32], x2[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = 0.f;
-                    // four units' rows in flight per round (the loads are
-                    // independent), added in unit order
-                    for (int sp0 = 0; sp0 < p.splits; sp0 += 4) {
-                        float4 f[4][8];
+                    // SU units' rows in flight per round (the loads are
+                    // independent), added in unit order; two for the epilogue
+                    // that also produces H, whose registers are fuller
+                    constexpr int SU = EPI == EPI_DGELU_H ? 2 : 4;
+                    for (int sp0 = 0; sp0 < p.splits; sp0 += SU) {
+                        float4 f[SU][8];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
+                        for (int u = 0; u < SU; ++u) {
                             if (sp0 + u < p.splits) {
                                 const int vblk = (u0 + sp0 + u) * TL::kHalves + (c >> 3);
                                 const long long r =
@@ -958,7 +990,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                             }
                         }
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
+                        for (int u = 0; u < SU; ++u) {
                             if (sp0 + u < p.splits) {
 #pragma unroll
                                 for (int q = 0; q < 8; ++q) {
@@ -975,6 +1007,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     load_in0<EPI>(p, part, in_row, m, n, in);
                     epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, in);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
+                    if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
+                        if (p.colsum_part) warp_column_sums(p, g, m0 + quarter * 32, m, n, lane, x);
+                    }
                 }
                 if (warp == 2 && lane == 0) p.counters[slot] = 0;  // ready for the next launch
             }

@@ -107,6 +107,11 @@ struct GemmParams {
     int out_rows_per_part;   // rows per output chunk for PART_ROW
     int bias_group_stride;   // bias offset per group (EPI_BIAS_GELU, EPI_BIAS)
     DropoutParams drop;      // EPI_BIAS_DROP_RES: mask of element (m, n) = Philox word of m * N + n
+    // EPI_DGELU / EPI_DGELU_H: column sums of the fp32 output (the bias gradient
+    // db1), one row per 32-row group of the output: colsum_part[r / 32][g * N + n]
+    // (null: none)
+    float* colsum_part;
+    long long colsum_ld;     // floats per partial row (groups x N)
     // control
     unsigned int* err;
     unsigned long long timeout_ns;

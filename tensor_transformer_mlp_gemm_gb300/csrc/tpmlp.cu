@@ -276,7 +276,10 @@ Layout layout_of(const tpmlp_dims& d) {
     L.h = act;
     L.dy = 2 * act;
     L.part1 = 3 * act;
-    L.part2 = L.part1 + align256(colsum_scratch_bytes(d.ffn));
+    // db1: the dH GEMM's epilogue writes one row of column sums per 32 token rows
+    const size_t groups = static_cast<size_t>((d.tokens + 31) / 32);
+    const size_t db1_part = groups * static_cast<size_t>(d.ffn) * sizeof(float);
+    L.part2 = L.part1 + align256(db1_part > 0 ? db1_part : 256);
     L.split_part = L.part2 + align256(colsum_scratch_bytes(d.hidden));
     L.split_cnt = L.split_part + split_part_bytes();
     L.total = L.split_cnt + split_cnt_bytes();
@@ -462,6 +465,9 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
         p.ld_in = s.fi;
         p.out_part = PART_GROUP;
         p.out_rows_per_part = 0;
+        // db1 partial sums: one row per 32 token rows, the t shards side by side
+        p.colsum_part = reinterpret_cast<float*>(R.part1);
+        p.colsum_ld = s.f;
         if (!attach_split(p, R)) return TPMLP_ERR_UNSUPPORTED;
         TPMLP_CUDA(timed(TPMLP_KERNEL_DGRAD_H, 1, st,
                          [&] {
@@ -539,20 +545,14 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
         TPMLP_CUDA(timed(TPMLP_KERNEL_WGRAD_A, 1, st,
                          [&] { return launch_wgrad(p, st); }));
     }
-    // db1 = column sums of dY (per shard block), db2 = column sums of dZ
+    // db1 = column sums of dY: the dH GEMM's epilogue summed each 32-row group
+    // of its fp32 output; here the groups are added.  db2 = column sums of dZ.
     {
-        ColsumParams c1;
-        std::memset(&c1, 0, sizeof(c1));
-        for (int i = 0; i < s.t; ++i) c1.src[i] = shard_ptr(dY, i, s);
-        c1.nparts = s.t;
-        c1.rows_per_part = s.T;
-        c1.ncols = s.fi;
-        c1.mode = CS_COLS_CONCAT;
-        c1.out = static_cast<float*>(db1);
-        c1.partial = reinterpret_cast<float*>(R.part1);
-        const dim3 g1 = colsum_plan(c1, dev->sm_count);
-        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, c1.splits > 1 ? 2 : 1, st,
-                         [&] { return launch_colsum(c1, g1, st, nullptr); }));
+        const long long groups = (s.T + 31) / 32;
+        TPMLP_CUDA(timed(TPMLP_KERNEL_BIAS_GRAD, 1, st, [&] {
+            return launch_colsum_f32(reinterpret_cast<const float*>(R.part1), groups, s.f, s.f,
+                                     static_cast<float*>(db1), st);
+        }));
 
         ColsumParams c2;
         std::memset(&c2, 0, sizeof(c2));

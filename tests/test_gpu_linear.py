@@ -127,9 +127,11 @@ def _assert_bitwise(a, b, what):
 
 def test_mlp_block_equals_its_linear_halves():
     """Column linear = the block's pre-activation Y; row linear on the block's
-    H = the block's Z; the linear backward calls reproduce the block's dX, dA,
-    db1 (from its dY) and dB (from its H and dZ) -- all bitwise, since both run
-    the same kernels in the same accumulation order."""
+    H = the block's Z; the linear backward calls reproduce the block's dX, dA
+    (from its dY), dB (from its H and dZ) and db2 -- all bitwise, since both
+    run the same kernels in the same accumulation order.  db1 agrees within
+    the parity gate: the block sums dY in fp32 inside its dH GEMM, before
+    rounding it to bf16, while the linear layer sums the bf16 dY it is given."""
     from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
     from tensor_transformer_mlp_gemm_gb300.linear import DeviceLinear
     w = custom(512, 256, 1024, 4, seq_chunks=4)
@@ -153,7 +155,8 @@ def test_mlp_block_equals_its_linear_halves():
     _assert_bitwise(col.dX, blk.dX, "dX")
     _assert_bitwise(col.dW, blk.dA, "dA")
     _assert_bitwise(row.dW, blk.dB, "dB")
-    assert torch.equal(col.db, blk.db1) and torch.equal(row.db, blk.db2)
+    assert torch.equal(row.db, blk.db2)
+    gate("db1 block vs column linear", blk.db1.cpu(), col.db.cpu())
 
 
 def _rows_of(lin, which, rows):
