@@ -698,12 +698,14 @@ class SpRunner(MlpRunner):
         self.flops_step = 12.0 * T * h * f
         self.gemm_kinds = ("column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a")
         self.gemm_flops = 2.0 * T * h * f
-        self.colsum_bytes = ((T + 31) // 32) * f * 4 + f * 4 + T * h * 2 + h * 4
+        # bias-gradient kernels: only db1's finish here (db2 comes out of the dropout pass)
+        self.colsum_bytes = ((T + 31) // 32) * f * 4 + f * 4
         # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes
         # dX (the dgamma / dbeta pass re-reads X and dLN(X): not counted, algorithmic bytes only)
         self.ln_fwd_bytes = 2 * T * h * 2
         self.ln_bwd_bytes = 4 * T * h * 2
-        self.dropout_bytes = 2 * T * h * 2
+        # dropout backward reads dOut and the mask's bits, writes dZ (and db2 from it)
+        self.dropout_bytes = 2 * T * h * 2 + T * ((h + 31) // 32) * 4 + h * 4
         self.l2_note = (f"inputs larger than L2 (bf16 weights {2 * h * f * 2 / 1e9:.2f} GB, "
                         f"activations {(3 * T * f + 4 * T * h) * 2 / 1e9:.2f} GB per step)")
         self.ins, self.outs = ("X", "dOut"), ("Out", "dX")

@@ -267,16 +267,19 @@ tpmlp_status tpmlp_row_linear_backward(const tpmlp_linear_dims* dims,
  * The same element keeps the same mask in the forward and the backward call.
  *
  * The forward pass runs LN per token chunk, then the block on LN(X) with the
- * dropout and the residual add fused into the row GEMM's epilogue; the
- * backward pass undoes the dropout on dOut, runs the block's backward pass,
- * then LN's backward with the residual gradient dOut added:
+ * dropout and the residual add fused into the row GEMM's epilogue, which also
+ * stores the mask as bits in the workspace; the backward pass undoes the
+ * dropout on dOut from those bits (summing dZ's columns into db2 on the way),
+ * runs the block's backward pass, then LN's backward with the residual
+ * gradient dOut added:
  *   dX = LN'(dXn) + dOut,  dgamma = sum_r dXn * xhat,  dbeta = sum_r dXn
  * Layouts, chunking, conventions and errors as tpmlp_forward / tpmlp_backward,
  * with h <= 16384 (else TPMLP_ERR_UNSUPPORTED), eps >= 0 and 0 <= p < 1
  * (else TPMLP_ERR_INVALID_ARG).  gamma, beta [h] bf16; dgamma, dbeta [h] fp32.
  * The workspace (tpmlp_sp_workspace_bytes) holds the block's workspace plus
- * LN(X), the row statistics, dZ and the gradient of LN(X); it must be kept
- * from the forward call to the matching backward call. */
+ * LN(X), the row statistics, the dropout mask's bits (T x ceil(h / 32) 32-bit
+ * words), dZ and the gradient of LN(X); it must be kept from the forward call
+ * to the matching backward call. */
 typedef struct {
     float eps;           /* LayerNorm epsilon (e.g. 1e-5) */
     double dropout_p;    /* probability of dropping an element, 0 <= p < 1 */
@@ -422,8 +425,8 @@ enum {
     TPMLP_KERNEL_LINEAR_DGRAD = 8,  /* linear layers: dX = sum_i dY_i.W_i^T, dX_i = dZ.W_i^T */
     TPMLP_KERNEL_LINEAR_WGRAD = 9,  /* linear layers: dW_i */
     TPMLP_KERNEL_LAYERNORM_FWD = 10,  /* sequence-parallel sublayer: LN(X) and row statistics */
-    TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (3 launches) */
-    TPMLP_KERNEL_DROPOUT_BWD = 12,    /* sequence-parallel sublayer: dZ from dOut and the mask */
+    TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (4 launches) */
+    TPMLP_KERNEL_DROPOUT_BWD = 12,    /* sequence-parallel sublayer: dZ from dOut and the mask, db2 (2 launches) */
     TPMLP_KERNEL_KINDS = 13
 };
 tpmlp_status tpmlp_profile_begin(int capacity);

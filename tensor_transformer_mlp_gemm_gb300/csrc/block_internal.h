@@ -56,12 +56,13 @@ tpmlp_status run_forward(const Shapes& s, const abi::DeviceInfo* dev, const void
                          const void* const* A_shards, const void* b1,
                          const void* const* B_shards, const void* b2, void* const* Z,
                          const Regions& R, cudaStream_t st, const RowEpilogue* ep);
-// The backward pass; recompute = true rebuilds H from the saved Y.
+// The backward pass; recompute = true rebuilds H from the saved Y; with
+// db2_given the caller has already written db2 (its column sums of dZ).
 tpmlp_status run_backward(const Shapes& s, const abi::DeviceInfo* dev, const void* const* dZ,
                           const void* const* X, const void* const* A_shards,
                           const void* const* B_shards, void* const* dX, void* const* dA_shards,
                           void* db1, void* const* dB_shards, void* db2, const Regions& R,
-                          bool recompute, cudaStream_t st);
+                          bool recompute, cudaStream_t st, bool db2_given = false);
 
 }  // namespace block
 }  // namespace tpmlp

@@ -145,8 +145,10 @@ dim3 colsum_plan(ColsumParams& p, int sm_count) {
     const long long total_rows =
         p.mode == CS_ROWS_CONCAT ? p.rows_per_part * p.nparts : p.rows_per_part;
     const long long base = static_cast<long long>(strips) * groups;
-    long long splits = (4LL * sm_count + base - 1) / base;
-    const long long max_by_rows = total_rows / 256 > 0 ? total_rows / 256 : 1;
+    // many short CTAs (about sixteen per SM, at least 128 rows each), so the
+    // last of them to start ends soon after the rest
+    long long splits = (16LL * sm_count + base - 1) / base;
+    const long long max_by_rows = total_rows / 128 > 0 ? total_rows / 128 : 1;
     if (splits > max_by_rows) splits = max_by_rows;
     if (splits > CS_MAX_SPLITS) splits = CS_MAX_SPLITS;
     if (splits < 1) splits = 1;

@@ -378,6 +378,7 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
         if (m < p.M) {
             const uint64_t e0 = static_cast<uint64_t>(m) * static_cast<uint64_t>(p.N) +
                                 static_cast<uint64_t>(n);
+            uint32_t bits = 0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const PhiloxOut o = philox4x32_10(p.drop.offset + e0 / 4 + q, p.drop.seed);
@@ -385,8 +386,12 @@ __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int pa
                 for (int j = 0; j < 4; ++j) {
                     const bool keep = static_cast<uint64_t>(o.w[j]) < p.drop.thresh;
                     x[4 * q + j] = keep ? x[4 * q + j] * p.drop.scale : 0.0f;
+                    bits |= (keep ? 1u : 0u) << (4 * q + j);
                 }
             }
+            // the mask's bits for the backward pass (n is a multiple of 32)
+            if (p.drop.mask)
+                p.drop.mask[static_cast<long long>(m) * p.drop.mask_words + n / 32] = bits;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 if (n + 8 * q < p.N) {

@@ -2,13 +2,15 @@
 // sequence-parallel sublayer (see layernorm.cuh).  One CTA of 256 threads per
 // token row in the forward pass and in the dX pass of the backward; each
 // thread holds up to eight 8-element vectors of its row in registers, so every
-// input is read once and every output written once.  dgamma and dbeta come
-// from a separate column-reduction pass over dXn and X.
+// input is read once and every output written once.  dgamma and dbeta come from a separate
+// column-reduction pass over dXn and X.  The dropout backward reads the keep
+// bits the forward pass stored and sums dZ's columns (db2) as it goes.
 // Reductions run warp-shuffle then one warp over the partial sums, always in
 // the same order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "colsum.cuh"
 #include "layernorm.cuh"
 
 namespace tpmlp {
@@ -120,29 +122,84 @@ __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardP
     }
 }
 
-// grid (T, ceil(h / 8 / LN_THREADS)): one 8-element vector per thread
-__global__ void __launch_bounds__(LN_THREADS) dropout_backward_kernel(const DropoutBackwardParams p) {
-    const long long r = blockIdx.x;
-    const int c = (blockIdx.y * LN_THREADS + threadIdx.x) * 8;
-    if (c >= p.h) return;
+// One 8-element vector of the dropout backward pass: dOut at (r, col) and the
+// keep bits of its 32-column word.
+__device__ __forceinline__ void dropout_load(const DropoutBackwardParams& p, long long r, int col,
+                                             uint4& u, uint32_t& word) {
     int j;
-    const long long rr = chunk_row(r, p.dout.rows, j);
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.dout.in[j]) + rr * p.h + c;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dz[j]) + rr * p.h + c;
-    const uint64_t e0 = static_cast<uint64_t>(r) * static_cast<uint64_t>(p.h) +
-                        static_cast<uint64_t>(c);  // a multiple of 8
+    const long long off = chunk_row(r, p.dout.rows, j) * p.h + col;
+    u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout.in[j]) + off));
+    word = __ldg(p.drop.mask + r * p.drop.mask_words + col / 32);
+}
+
+// dZ for that vector, stored; its bf16 values added to acc.
+__device__ __forceinline__ void dropout_apply(const DropoutBackwardParams& p, long long r, int col,
+                                              const uint4& u, uint32_t word, float (&acc)[8]) {
+    int j;
+    const long long off = chunk_row(r, p.dout.rows, j) * p.h + col;
+    const uint32_t bits = word >> (col & 31);
     float f[8];
-    unpack8(*reinterpret_cast<const uint4*>(src), f);
+    unpack8(u, f);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const PhiloxOut o = philox4x32_10(p.drop.offset + e0 / 4 + q, p.drop.seed);
+    for (int k = 0; k < 8; ++k) f[k] = ((bits >> k) & 1u) ? f[k] * p.drop.scale : 0.0f;
+    const uint4 o = pack8(f);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dz[j]) + off) = o;
+    float g[8];
+    unpack8(o, g);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const bool keep = static_cast<uint64_t>(o.w[k]) < p.drop.thresh;
-            f[4 * q + k] = keep ? f[4 * q + k] * p.drop.scale : 0.0f;
+    for (int k = 0; k < 8; ++k) acc[k] += g[k];
+}
+
+// dZ = keep ? dOut * scale : 0 from the keep bits the forward pass stored,
+// and the column sums of dZ (as rounded to bf16) per row split: CTA = a
+// 64-column strip x 32 row slots over the rows of split blockIdx.y; thread
+// (slot, vec) handles columns vec*8 .. vec*8+7 of rows slot, slot + 32, ...
+// (four rows' loads in flight), and the slots are added in order through
+// shared memory into part[split][col].
+__global__ void __launch_bounds__(LN_THREADS, 3) dropout_backward_kernel(const DropoutBackwardParams p,
+                                                                      long long T) {
+    constexpr int COLS = 64;
+    __shared__ float red[32][COLS + 1];
+    const int h = p.h;
+    const int vec = threadIdx.x & 7, slot = threadIdx.x >> 3;
+    const int col = blockIdx.x * COLS + vec * 8;
+    const long long r0 = static_cast<long long>(blockIdx.y) * p.rows_per_split;
+    const long long r1 = r0 + p.rows_per_split < T ? r0 + p.rows_per_split : T;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+    if (col < h) {
+        long long r = r0 + slot;
+        for (; r + 96 < r1; r += 128) {
+            uint4 u0, u1, u2, u3;
+            uint32_t w0, w1, w2, w3;
+            dropout_load(p, r, col, u0, w0);
+            dropout_load(p, r + 32, col, u1, w1);
+            dropout_load(p, r + 64, col, u2, w2);
+            dropout_load(p, r + 96, col, u3, w3);
+            dropout_apply(p, r, col, u0, w0, acc);
+            dropout_apply(p, r + 32, col, u1, w1, acc);
+            dropout_apply(p, r + 64, col, u2, w2, acc);
+            dropout_apply(p, r + 96, col, u3, w3, acc);
+        }
+        for (; r < r1; r += 32) {
+            uint4 u;
+            uint32_t w;
+            dropout_load(p, r, col, u, w);
+            dropout_apply(p, r, col, u, w, acc);
         }
     }
-    *reinterpret_cast<uint4*>(dst) = pack8(f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) red[slot][vec * 8 + k] = acc[k];
+    __syncthreads();
+    if (threadIdx.x < COLS) {
+        const int c = blockIdx.x * COLS + threadIdx.x;
+        if (c < h) {
+            float sum = 0.0f;
+            for (int k = 0; k < 32; ++k) sum += red[k][threadIdx.x];
+            p.part[static_cast<long long>(blockIdx.y) * h + c] = sum;
+        }
+    }
 }
 
 // Sum of two values over the CTA in one pass (both orders fixed).
@@ -281,20 +338,6 @@ __global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackw
     }
 }
 
-// dgamma[c] = sum_b part[b][0][c], dbeta[c] = sum_b part[b][1][c], b in order
-__global__ void ln_finish_kernel(const float* part, int splits, int h, float* dgamma,
-                                 float* dbeta) {
-    const int c = blockIdx.x * blockDim.x + threadIdx.x;
-    if (c >= h) return;
-    float g = 0.0f, b = 0.0f;
-    for (int k = 0; k < splits; ++k) {
-        g += part[static_cast<size_t>(k) * 2 * h + c];
-        b += part[static_cast<size_t>(k) * 2 * h + h + c];
-    }
-    dgamma[c] = g;
-    dbeta[c] = b;
-}
-
 // Vectors per thread for rows of h elements: the smallest of 1, 2, 4, 8 that covers h.
 int ln_vec(int h) {
     const int v = (h + 8 * LN_THREADS - 1) / (8 * LN_THREADS);
@@ -315,12 +358,23 @@ cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_
     return cudaGetLastError();
 }
 
-cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, cudaStream_t st) {
+int dropout_splits(long long T, long long h, int sm_count) {
+    const long long strips = (h + 63) / 64;
+    long long sp = (16LL * sm_count + strips - 1) / strips;
+    const long long by_rows = T / 128 > 0 ? T / 128 : 1;
+    if (sp > by_rows) sp = by_rows;
+    if (sp > LN_MAX_SPLITS) sp = LN_MAX_SPLITS;
+    return static_cast<int>(sp < 1 ? 1 : sp);
+}
+
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, float* db2,
+                                    cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
-    const int vecs = (p.h + 7) / 8;
-    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((vecs + LN_THREADS - 1) / LN_THREADS));
-    dropout_backward_kernel<<<grid, LN_THREADS, 0, st>>>(p);
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>((p.h + 63) / 64), static_cast<unsigned>(p.splits));
+    dropout_backward_kernel<<<grid, LN_THREADS, 0, st>>>(p, T);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_colsum_f32(p.part, p.splits, p.h, p.h, db2, st);
 }
 
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
@@ -340,8 +394,10 @@ cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int split
     ln_param_grad_kernel<<<grid, LN_THREADS, 0, st>>>(p, T);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    ln_finish_kernel<<<(p.h + 255) / 256, 256, 0, st>>>(p.part, splits, p.h, dgamma, dbeta);
-    return cudaGetLastError();
+    // dgamma = sum of part[s][0][:], dbeta = sum of part[s][1][:] over the splits
+    e = launch_colsum_f32(p.part, splits, 2LL * p.h, p.h, dgamma, st);
+    if (e != cudaSuccess) return e;
+    return launch_colsum_f32(p.part + p.h, splits, 2LL * p.h, p.h, dbeta, st);
 }
 
 }  // namespace tpmlp

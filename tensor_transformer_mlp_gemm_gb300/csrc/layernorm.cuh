@@ -4,7 +4,8 @@
 //   ln_forward:       Xn = (X - mean) * rstd * gamma + beta per token row, with
 //                     mean and rstd = 1 / sqrt(var + eps) (biased variance)
 //                     kept for the backward pass
-//   dropout_backward: dZ = keep ? dOut / (1 - p) : 0 (the forward's mask)
+//   dropout_backward: dZ = keep ? dOut / (1 - p) : 0 (the keep bits the
+//                     forward pass stored) and the column sums of dZ (db2)
 //   ln_backward:      dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dOut,
 //                     g = dXn * gamma (one CTA per token row), then dgamma =
 //                     sum dXn * xhat and dbeta = sum dXn as column sums over
@@ -45,8 +46,16 @@ struct DropoutBackwardParams {
     LnChunks dout;               // bf16 [rows, h] per chunk
     void* dz[LN_MAX_CHUNKS];     // bf16, same chunking
     int h;
-    DropoutParams drop;
+    DropoutParams drop;          // drop.mask: the keep bits the forward pass stored
+    float* part;                 // fp32 [splits][h] partial column sums of dZ
+    int splits;                  // row splits
+    long long rows_per_split;
 };
+
+// Row splits of the dropout backward pass (which also sums dZ's columns):
+// enough 64-column CTAs to cover the GPU about sixteen times, at least 128
+// rows per split, at most LN_MAX_SPLITS.
+int dropout_splits(long long T, long long h, int sm_count);
 
 struct LnBackwardParams {
     LnChunks x;                  // bf16 X (the sublayer input)
@@ -68,20 +77,24 @@ inline size_t ln_partial_bytes(long long h) {
     return static_cast<size_t>(LN_MAX_SPLITS) * 2 * static_cast<size_t>(h) * sizeof(float);
 }
 // Row splits of the dgamma / dbeta pass: enough 64-column CTAs to cover the
-// GPU about four times, at least 256 rows per split.
+// GPU about sixteen times (many short CTAs, so the last to start ends soon
+// after the rest), at least 128 rows per split.
 inline int ln_param_splits(long long T, long long h, int sm_count) {
     const long long strips = (h + 63) / 64;
-    long long s = (4LL * sm_count + strips - 1) / strips;
-    const long long by_rows = T / 256 > 0 ? T / 256 : 1;
+    long long s = (16LL * sm_count + strips - 1) / strips;
+    const long long by_rows = T / 128 > 0 ? T / 128 : 1;
     if (s > by_rows) s = by_rows;
     if (s > LN_MAX_SPLITS) s = LN_MAX_SPLITS;
     return static_cast<int>(s < 1 ? 1 : s);
 }
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st);
-cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, cudaStream_t st);
-// Three launches: dX per token row, the dgamma / dbeta partial column sums
-// over `splits` row splits, and their fixed-order finish.
+// Two launches: dZ with its per-split column sums, then db2 = their
+// fixed-order sum.
+cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, float* db2,
+                                    cudaStream_t st);
+// Four launches: dX per token row, the dgamma / dbeta partial column sums
+// over `splits` row splits, and their fixed-order finish (one per output).
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st);
 

@@ -42,12 +42,17 @@ __device__ __forceinline__ PhiloxOut philox4x32_10(uint64_t counter, uint64_t se
     return PhiloxOut{{c0, c1, c2, c3}};
 }
 
-// Dropout parameters as the kernels see them.
+// Dropout parameters as the kernels see them.  The forward pass draws the
+// mask and, when `mask` is set, also stores it as bits: bit n % 32 of word
+// row * mask_words + n / 32 is the keep decision of element (row, n), so the
+// backward pass reads 1 bit per element instead of drawing the mask again.
 struct DropoutParams {
     uint64_t seed;
     uint64_t offset;   // counter offset in 4-element blocks
     uint64_t thresh;   // keep iff word < thresh, thresh in [0, 2^32]
     float scale;       // 1 / (1 - p)
+    uint32_t* mask;    // [rows][mask_words] keep bits (null: not stored)
+    long long mask_words;
 };
 
 }  // namespace tpmlp

@@ -31,11 +31,14 @@ namespace {
 using namespace abi;
 using namespace block;
 
-// After the block's workspace: Xn | mean | rstd | dZ | dXn | LayerNorm partials.
+// After the block's workspace: Xn | mean | rstd | dZ | dXn | LayerNorm partials |
+// dropout keep bits | partial column sums of dZ.
 struct SpLayout {
     Layout blk;
-    size_t xn, mean, rstd, dz, dxn, part, total;
+    size_t xn, mean, rstd, dz, dxn, part, mask, dpart, total;
 };
+
+long long mask_words_of(long long h) { return (h + 31) / 32; }
 
 SpLayout sp_layout_of(const tpmlp_dims& d) {
     SpLayout L;
@@ -48,7 +51,11 @@ SpLayout sp_layout_of(const tpmlp_dims& d) {
     L.dz = L.rstd + row;
     L.dxn = L.dz + act;
     L.part = L.dxn + act;
-    L.total = L.part + align256(ln_partial_bytes(d.hidden));
+    L.mask = L.part + align256(ln_partial_bytes(d.hidden));
+    L.dpart = L.mask + align256(static_cast<size_t>(d.tokens) *
+                                static_cast<size_t>(mask_words_of(d.hidden)) * sizeof(uint32_t));
+    L.total = L.dpart + align256(static_cast<size_t>(LN_MAX_SPLITS) *
+                                 static_cast<size_t>(d.hidden) * sizeof(float));
     return L;
 }
 
@@ -147,6 +154,9 @@ TPMLP_API tpmlp_status tpmlp_sp_forward(const tpmlp_dims* dims, const tpmlp_sp_p
     RowEpilogue ep;
     ep.residual = X;
     ep.drop = dropout_of(*sp);
+    // the row GEMM's epilogue also stores the mask's bits for the backward pass
+    ep.drop.mask = reinterpret_cast<uint32_t*>(ws + L.mask);
+    ep.drop.mask_words = mask_words_of(s.h);
     return run_forward(s, dev, xn, A_shards, b1, B_shards, b2, Out, regions_of(ws, L.blk), st, &ep);
 }
 
@@ -199,11 +209,18 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_
     db.dout.rows = s.Tc;
     db.h = s.h;
     db.drop = dropout_of(*sp);
-    TPMLP_CUDA(timed(TPMLP_KERNEL_DROPOUT_BWD, 1, st,
-                     [&] { return launch_dropout_backward(db, s.T, st); }));
+    db.drop.mask = reinterpret_cast<uint32_t*>(ws + L.mask);  // written by the forward pass
+    db.drop.mask_words = mask_words_of(s.h);
+    db.part = reinterpret_cast<float*>(ws + L.dpart);
+    db.splits = dropout_splits(s.T, s.h, dev->sm_count);
+    db.rows_per_split = (s.T + db.splits - 1) / db.splits;
+    // dZ and, from the same pass, db2 = its column sums
+    TPMLP_CUDA(timed(TPMLP_KERNEL_DROPOUT_BWD, 2, st, [&] {
+        return launch_dropout_backward(db, s.T, static_cast<float*>(db2), st);
+    }));
 
     TPMLP_TRY(run_backward(s, dev, dz, xn, A_shards, B_shards, dxn, dA_shards, db1, dB_shards,
-                           db2, regions_of(ws, L.blk), false, st));
+                           db2, regions_of(ws, L.blk), false, st, /*db2_given=*/true));
 
     LnBackwardParams lb;
     std::memset(&lb, 0, sizeof(lb));
@@ -222,7 +239,7 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_
     lb.h = s.h;
     const int splits = ln_param_splits(s.T, s.h, dev->sm_count);
     lb.rows_per_block = (s.T + splits - 1) / splits;
-    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_BWD, 3, st, [&] {
+    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_BWD, 4, st, [&] {
         return launch_ln_backward(lb, s.T, splits, static_cast<float*>(dgamma),
                                   static_cast<float*>(dbeta), st);
     }));

@@ -432,7 +432,7 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
                           const void* const* X, const void* const* A_shards,
                           const void* const* B_shards, void* const* dX, void* const* dA_shards,
                           void* db1, void* const* dB_shards, void* db2, const Regions& R,
-                          bool recompute, cudaStream_t st) {
+                          bool recompute, cudaStream_t st, bool db2_given) {
     const void* Y = R.y;
     const void* H = R.h;
     const void* dY = R.dy;
@@ -554,6 +554,7 @@ tpmlp_status run_backward(const Shapes& s, const DeviceInfo* dev, const void* co
                                      static_cast<float*>(db1), st);
         }));
 
+        if (db2_given) return TPMLP_OK;
         ColsumParams c2;
         std::memset(&c2, 0, sizeof(c2));
         for (int j = 0; j < s.chunks; ++j) c2.src[j] = dZ[j];

@@ -17,11 +17,11 @@ the first left in the shared array):
     launch; an empty batch gives zeros.
 
 The entry point caps its row splits so that the partial sums fit the array
-(splits x cols <= 2^20).  The split plan asks for about 4 x SMs / (cols / 64)
-splits, so on this GPU (152 SMs) splits x cols stays below 4 x 152 x 64 + cols
-and the cap never binds; the cases above still run every split count the plan
-makes (1 split at 2^20 and 65536 columns, 11 at 3001 x 1000, 16 at 4096 x 1024,
-38 at 65536 x 1000).
+(splits x cols <= 2^20).  The split plan asks for about 16 x SMs / (cols / 64)
+splits (at most one per 128 rows, at most 64), so on this GPU (152 SMs) splits x
+cols stays below 16 x 152 x 64 + cols and the cap never binds; the cases above
+run split counts from 1 to 64 (1 at 2^20 columns, 3 at 4096 x 65536, 23 at
+3001 x 1000, 32 at 4096 x 1024, 64 at 65536 x 1000).
 
 This file is collected last on purpose and also passes when run alone.
 """
