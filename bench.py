@@ -81,6 +81,11 @@ def parse_args():
     ap.add_argument("--sp-layer", action="store_true",
                     help="run the sequence-parallel sublayer Out = X + Dropout(MLP(LN(X))) around "
                          "the MLP workload (dropout p = 0.1, eps = 1e-5)")
+    ap.add_argument("--sp-explicit-copy", action="store_true",
+                    help="sequence-parallel workloads: gather the token chunks into one tensor and "
+                         "scatter the outputs back with explicit copies (tpmlp_sp_gather / "
+                         "tpmlp_sp_scatter) around the un-chunked block, instead of addressing the "
+                         "chunks through per-chunk tensor maps (the ablation of the copy-free path)")
     ap.add_argument("--recompute", action="store_true",
                     help="selective recompute: keep only Y between passes, rebuild H in backward")
     ap.add_argument("--split-min-kblocks", type=int, default=None,
@@ -673,6 +678,52 @@ class MlpRunner:
                              blk.db1, blk.dB, blk.db2, stream)
 
 
+class MlpCopyRunner(MlpRunner):
+    """The sequence-parallel block with explicit copies: X and dZ arrive as
+    token chunks, are gathered into one [T, h] tensor each, the block runs
+    un-chunked, and Z and dX are scattered back to chunks."""
+
+    def __init__(self, args, dev):
+        super().__init__(args, dev)
+        import torch
+        from dataclasses import replace
+        from tensor_transformer_mlp_gemm_gb300.block import DeviceBlock
+        w = self.w
+        if w.seq_chunks < 2:
+            raise SystemExit("--sp-explicit-copy needs a workload with token chunks")
+        self.chunked = self.blk            # its X, dZ, Z, dX chunk buffers face the caller
+        self.blk = DeviceBlock(replace(w, seq_chunks=1), self.inputs, device=dev,
+                               recompute=args.recompute)
+        self.cdims = self.chunked.dims
+        self.h = w.hidden
+        self.torch = torch
+
+    def config(self):
+        c = super().config()
+        c["sp_addressing"] = "explicit gather / scatter copies around the un-chunked block"
+        return c
+
+    def buffers(self, name):
+        return getattr(self.chunked, name)
+
+    def step(self, stream):
+        self.forward({"X": self.chunked.X, "Z": self.chunked.Z}, stream)
+        self.backward({"dZ": self.chunked.dZ, "X": self.chunked.X, "dX": self.chunked.dX},
+                      stream)
+
+    def forward(self, B, stream):
+        b, blk = self.binding, self.blk
+        b.tpmlp_sp_gather(self.cdims, B["X"], self.h, blk.X[0], stream)
+        super().forward({"X": blk.X, "Z": blk.Z}, stream)
+        b.tpmlp_sp_scatter(self.cdims, blk.Z[0], self.h, B["Z"], stream)
+
+    def backward(self, B, stream):
+        b, blk = self.binding, self.blk
+        b.tpmlp_sp_gather(self.cdims, B["dZ"], self.h, blk.dZ[0], stream)
+        super().backward({"dZ": blk.dZ, "X": blk.X, "dX": blk.dX}, stream)
+        b.tpmlp_sp_scatter(self.cdims, blk.dX[0], self.h, B["dX"], stream)
+
+
 def sp_config():
     return {"sublayer": "Out = X + Dropout(MLP(LN(X))), LayerNorm and dropout per token chunk",
             "layernorm_eps": SP_EPS, "dropout_p": SP_P, "dropout_seed": SP_SEED,
@@ -784,6 +835,8 @@ def run_ours(args, torch):
         run = LinearRunner(args, dev)
     elif args.sp_layer:
         run = SpRunner(args, dev)
+    elif args.sp_explicit_copy:
+        run = MlpCopyRunner(args, dev)
     else:
         run = MlpRunner(args, dev)
     w = run.w

@@ -382,6 +382,25 @@ tpmlp_status tpmlp_set_wait_timeout_ns(uint64_t ns);
 tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b, void* c,
                                          uint64_t timeout_ns, void* stream);
 
+/* Explicit sequence-parallel gather and scatter ("Megatron-LM：NVIDIA 的大规模
+ * 并行训练方案", 并行训练范式 / 序列并行: the tensor-parallel block gathers the
+ * sequence chunks before its column-parallel GEMM and reduce-scatters its
+ * output to them after the row-parallel GEMM).  tpmlp_forward / tpmlp_backward
+ * do both without copies, through one tensor map per chunk and an epilogue that
+ * writes each row into its chunk; these calls make the copies explicit.
+ *   tpmlp_sp_gather:  out[T, cols] = concatenation along tokens of the
+ *                     dims->seq_chunks chunks [T / seq_chunks, cols]
+ *   tpmlp_sp_scatter: chunk j = rows [j T / seq_chunks, (j + 1) T / seq_chunks)
+ *                     of in[T, cols]
+ * bf16 (any 2-byte element), row-major, cols a multiple of 8 (else
+ * TPMLP_ERR_UNSUPPORTED), 16-byte-aligned device pointers, at most 8 chunks;
+ * dims->tokens and dims->seq_chunks are read, the rest of dims is not.  One
+ * kernel on `stream`, asynchronous; nothing is allocated. */
+tpmlp_status tpmlp_sp_gather(const tpmlp_dims* dims, const void* const* chunks, int64_t cols,
+                             void* out, void* stream);
+tpmlp_status tpmlp_sp_scatter(const tpmlp_dims* dims, const void* in, int64_t cols,
+                              void* const* chunks, void* stream);
+
 /* Column sums of one bf16 matrix [rows, cols] into fp32 out[cols] -- the
  * reduction tpmlp_backward uses for its bias gradients (db2 is the column
  * sums of dZ) -- for callers that cannot allocate device memory.  The pages
@@ -427,7 +446,8 @@ enum {
     TPMLP_KERNEL_LAYERNORM_FWD = 10,  /* sequence-parallel sublayer: LN(X) and row statistics */
     TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (4 launches) */
     TPMLP_KERNEL_DROPOUT_BWD = 12,    /* sequence-parallel sublayer: dZ from dOut and the mask, db2 (2 launches) */
-    TPMLP_KERNEL_KINDS = 13
+    TPMLP_KERNEL_SP_COPY = 13,        /* tpmlp_sp_gather / tpmlp_sp_scatter */
+    TPMLP_KERNEL_KINDS = 14
 };
 tpmlp_status tpmlp_profile_begin(int capacity);
 int tpmlp_profile_end(double* ms, int* launches, int nkinds);

@@ -27,7 +27,7 @@ TPMLP_ERR_UNSUPPORTED = 2
 TPMLP_ERR_CUDA = 3
 TPMLP_ERR_TIMEOUT = 4
 
-KERNEL_KINDS = 13
+KERNEL_KINDS = 14
 
 # every symbol include/tpmlp.h declares
 EXPORTED = (
@@ -40,7 +40,7 @@ EXPORTED = (
     "tpmlp_row_linear_forward", "tpmlp_row_linear_backward",
     "tpmlp_sp_workspace_bytes", "tpmlp_sp_workspace_layout", "tpmlp_sp_forward", "tpmlp_sp_backward",
     "tpmlp_set_head_prefetch", "tpmlp_map_cache_stats", "tpmlp_selftest_map_cache",
-    "tpmlp_set_wide_tiles",
+    "tpmlp_set_wide_tiles", "tpmlp_sp_gather", "tpmlp_sp_scatter",
 )
 
 
@@ -94,6 +94,10 @@ _lib.tpmlp_map_cache_stats.restype = ctypes.c_int
 _lib.tpmlp_map_cache_stats.argtypes = [_u64p, _u64p, _u64p]
 _lib.tpmlp_selftest_map_cache.restype = ctypes.c_int
 _lib.tpmlp_selftest_map_cache.argtypes = [_u64p, ctypes.c_int]
+_lib.tpmlp_sp_gather.restype = ctypes.c_int
+_lib.tpmlp_sp_gather.argtypes = [_dims_p, _vpp, ctypes.c_int64, _vp, _vp]
+_lib.tpmlp_sp_scatter.restype = ctypes.c_int
+_lib.tpmlp_sp_scatter.argtypes = [_dims_p, _vp, ctypes.c_int64, _vpp, _vp]
 _lib.tpmlp_status_string.restype = ctypes.c_char_p
 _lib.tpmlp_status_string.argtypes = [ctypes.c_int]
 _lib.tpmlp_sync_check.restype = ctypes.c_int
@@ -294,6 +298,18 @@ def tpmlp_profile_end() -> tuple[dict, dict]:
     names = [tpmlp_kernel_name(k) for k in range(KERNEL_KINDS)]
     return ({names[k]: ms[k] for k in range(KERNEL_KINDS)},
             {names[k]: cnt[k] for k in range(KERNEL_KINDS)})
+
+
+def tpmlp_sp_gather(dims, chunks, cols: int, out, stream=None) -> None:
+    """out [T, cols] = the seq_chunks chunks concatenated along tokens."""
+    _check(_lib.tpmlp_sp_gather(ctypes.byref(dims), _arr(chunks), int(cols), _ptr(out),
+                                _stream(stream)), "tpmlp_sp_gather")
+
+
+def tpmlp_sp_scatter(dims, src, cols: int, chunks, stream=None) -> None:
+    """The seq_chunks chunks = the token-row blocks of src [T, cols]."""
+    _check(_lib.tpmlp_sp_scatter(ctypes.byref(dims), _ptr(src), int(cols), _arr(chunks),
+                                 _stream(stream)), "tpmlp_sp_scatter")
 
 
 def tpmlp_column_sums_noalloc(src, rows: int, cols: int, out, stream=None) -> int:

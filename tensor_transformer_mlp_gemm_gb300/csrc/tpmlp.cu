@@ -922,6 +922,7 @@ TPMLP_API const char* tpmlp_kernel_name(int kind) {
         case TPMLP_KERNEL_LAYERNORM_FWD: return "layernorm_fwd";
         case TPMLP_KERNEL_LAYERNORM_BWD: return "layernorm_bwd";
         case TPMLP_KERNEL_DROPOUT_BWD: return "dropout_bwd";
+        case TPMLP_KERNEL_SP_COPY: return "sp_copy";
     }
     return "unknown";
 }

@@ -55,7 +55,7 @@ def test_status_strings(binding):
     assert [binding.tpmlp_kernel_name(k) for k in range(binding.KERNEL_KINDS)] == [
         "column_fwd", "row_fwd", "dgrad_h", "dgrad_x", "wgrad_b", "wgrad_a", "bias_grad",
         "linear_fwd", "linear_dgrad", "linear_wgrad", "layernorm_fwd", "layernorm_bwd",
-        "dropout_bwd"]
+        "dropout_bwd", "sp_copy"]
 
 
 def test_workspace_bytes(binding):
@@ -258,3 +258,23 @@ def test_tensor_map_cache_logic(binding):
     assert lib.tpmlp_selftest_map_cache(None, 8) == binding.TPMLP_ERR_INVALID_ARG
     st = binding.tpmlp_map_cache_stats()
     assert set(st) == {"hits", "misses", "entries"}
+
+
+def test_sp_copy_validation(binding):
+    """Argument checks of the explicit sequence-parallel gather / scatter
+    (before any device work)."""
+    lib = binding.library()
+    arr = lambda n: (ctypes.c_void_p * n)(*([0x1000] * n))
+    d = binding.make_dims(512, 256, 1024, 4, 4)
+    assert lib.tpmlp_sp_gather(None, arr(4), 256, 0x1000, None) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_sp_gather(ctypes.byref(d), arr(4), 0, 0x1000, None) == \
+        binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_sp_gather(ctypes.byref(d), arr(4), 12, 0x1000, None) == \
+        binding.TPMLP_ERR_UNSUPPORTED                      # cols not a multiple of 8
+    assert lib.tpmlp_sp_gather(ctypes.byref(d), None, 256, 0x1000, None) == \
+        binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_sp_scatter(ctypes.byref(d), 0x1002, 256, arr(4), None) == \
+        binding.TPMLP_ERR_UNSUPPORTED                      # misaligned
+    d9 = binding.make_dims(512, 256, 1024, 4, 9)
+    assert lib.tpmlp_sp_scatter(ctypes.byref(d9), 0x1000, 256, arr(9), None) == \
+        binding.TPMLP_ERR_UNSUPPORTED                      # more than 8 chunks

@@ -339,3 +339,37 @@ def test_wide_tiles_match_narrow():
     for i in range(w.t):
         gate(f"dA[{i}] wide vs narrow", wide.dA[i].cpu(), narrow.dA[i].cpu())
         gate(f"dB[{i}] wide vs narrow", wide.dB[i].cpu(), narrow.dB[i].cpu())
+
+
+def test_explicit_sp_gather_scatter():
+    """tpmlp_sp_gather / tpmlp_sp_scatter: the gathered tensor is the chunks'
+    concatenation, the scatter its inverse, and gather -> un-chunked block ->
+    scatter gives the chunk-addressed block's outputs bitwise."""
+    from dataclasses import replace
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    w = custom(512, 264, 1056, 4, seq_chunks=4)
+    inputs = make_inputs(w, 19)
+    sp = _block(w, inputs)
+    sp.step()
+    plain = _block(replace(w, seq_chunks=1), inputs)
+    g = GuardBands()
+    g.guard(plain, ["X", "dZ"])
+    binding.tpmlp_sp_gather(sp.dims, sp.X, w.hidden, plain.X[0])
+    binding.tpmlp_sp_gather(sp.dims, sp.dZ, w.hidden, plain.dZ[0])
+    torch.cuda.synchronize()
+    g.check()
+    assert torch.equal(plain.X[0], torch.cat(sp.X, 0))
+    assert torch.equal(plain.dZ[0], torch.cat(sp.dZ, 0))
+    plain.step()
+    Zc = [torch.empty_like(z) for z in sp.Z]
+    dXc = [torch.empty_like(x) for x in sp.dX]
+    g2 = GuardBands()
+    holder = type("H", (), {})()
+    holder.Zc, holder.dXc = Zc, dXc
+    g2.guard(holder, ["Zc", "dXc"])
+    binding.tpmlp_sp_scatter(sp.dims, plain.Z[0], w.hidden, holder.Zc)
+    binding.tpmlp_sp_scatter(sp.dims, plain.dX[0], w.hidden, holder.dXc)
+    assert binding.tpmlp_sync_check() == binding.TPMLP_OK
+    g2.check()
+    _assert_bitwise(holder.Zc, sp.Z, "Z")
+    _assert_bitwise(holder.dXc, sp.dX, "dX")
