@@ -940,6 +940,24 @@ def run_ours(args, torch):
             kernels[name]["tflops"] = run.gemm_flops / (kernels[name]["ms_per_launch"] / 1e3) / 1e12
     launches_per_step = sum(kcount.values()) / args.steps
 
+    # The same eager steps without the per-kernel event pairs (two event
+    # records per launch cost host time that layers of a few hundred tokens see
+    # in their step time); reported beside the main line, not instead of it.
+    plain_events = None
+    if graph is None:
+        n_plain = min(args.steps, 200)
+        e6 = torch.cuda.Event(enable_timing=True)
+        e7 = torch.cuda.Event(enable_timing=True)
+        barrier(dist, torch)
+        e6.record(stream)
+        for _ in range(n_plain):
+            run.step(stream)
+        e7.record(stream)
+        barrier(dist, torch)
+        ms_plain = max_over_ranks(dist, torch, e6.elapsed_time(e7))
+        plain_events = {"value": flops_step * n_plain * world / (ms_plain / 1e3) / 1e12,
+                        "unit": "TFLOP/s", "ms_per_step": ms_plain / n_plain, "steps": n_plain}
+
     # Sustained sub-record: at least SUSTAINED_MIN_S of back-to-back steps, long
     # enough for the power cap to set the clock, with its own clock record.
     sustained = None
@@ -1073,6 +1091,7 @@ def run_ours(args, torch):
                                      "theoretical": (value / world / theo["tflops"]) if theo else None,
                                      "theoretical_peak": theo},
                 "roofline": roof, "kernels": kernels, "sustained": sustained,
+                "eager_without_kernel_events": plain_events,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "cublas_reference": cublas,
                 "clocks": clocks, "gpu_launches": int(sum(kcount.values())),

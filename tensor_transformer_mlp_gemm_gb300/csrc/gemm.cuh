@@ -348,20 +348,38 @@ __device__ __forceinline__ void load_in0(const GemmParams& p, int part, long lon
     }
 }
 
+// Epilogues that add a bias per output column.
+template <int EPI>
+struct EpiReadsBias {
+    static constexpr bool value = EPI == EPI_BIAS_GELU || EPI == EPI_BIAS || EPI == EPI_BIAS_DROP_RES;
+};
+
+// The bias of columns [n, n + 32) of group g as four 16-byte vectors (every
+// lane reads the same ones); issued a chunk ahead like load_in0.
+template <int EPI>
+__device__ __forceinline__ void load_bias(const GemmParams& p, int g, int n, uint4 (&b)[4]) {
+    if constexpr (EpiReadsBias<EPI>::value) {
+        const __nv_bfloat16* src =
+            static_cast<const __nv_bfloat16*>(p.bias) + n + g * p.bias_group_stride;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (n + 8 * q < p.N) b[q] = __ldg(reinterpret_cast<const uint4*>(src + 8 * q));
+    }
+}
+
 // Elementwise work on one thread's 32 values: row m, columns [n, n + 32);
-// `in` holds the second input (load_in0) for the epilogues that read one.
+// `in` holds the second input (load_in0) for the epilogues that read one,
+// `bias` the columns' bias (load_bias) for those that add one.
 template <int EPI>
 __device__ __forceinline__ void epilogue_math(const GemmParams& p, int g, int part, long long row,
                                               int m, int n, float (&x)[32], float (&x2)[32],
-                                              const uint4 (&in)[4]) {
-    if constexpr (EPI == EPI_BIAS_GELU || EPI == EPI_BIAS || EPI == EPI_BIAS_DROP_RES) {
-        const __nv_bfloat16* b =
-            static_cast<const __nv_bfloat16*>(p.bias) + n + g * p.bias_group_stride;
+                                              const uint4 (&in)[4], const uint4 (&bias)[4]) {
+    if constexpr (EpiReadsBias<EPI>::value) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (n + 8 * q < p.N) {
                 float bf[8];
-                unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(b + 8 * q)), bf);
+                unpack_bf16x8(bias[q], bf);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) x[8 * q + j] += bf[j];
             }
@@ -855,7 +873,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // the second input of the first chunk is read before the accumulator is ready
             uint4 pre[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                             make_uint4(0, 0, 0, 0)};
-            if (it.unit < 0) load_in0<EPI>(p, part, in_row, m, n0, pre);
+            uint4 bpre[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                             make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (it.unit < 0) {
+                load_in0<EPI>(p, part, in_row, m, n0, pre);
+                if constexpr (EPI != EPI_BIAS_DROP_RES) load_bias<EPI>(p, g, n0, bpre);
+            }
             // Waits for accumulator part b (TN = 256: accumulator b; TN = 512:
             // half b); all four epilogue warps give up together (they share
             // named barriers).
@@ -904,15 +927,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(taddr + c * EPI_CHUNK, v);
                     uint4 cur[4] = {pre[0], pre[1], pre[2], pre[3]};
-                    if (c + 1 < NCH)  // next chunk's second input, in flight meanwhile
+                    uint4 curb[4] = {bpre[0], bpre[1], bpre[2], bpre[3]};
+                    // the next chunk's second input and bias, in flight meanwhile (the
+                    // dropout epilogue, short of registers, reads its bias when used)
+                    if (c + 1 < NCH) {
                         load_in0<EPI>(p, part, in_row, m, n0 + (c + 1) * EPI_CHUNK, pre);
+                        if constexpr (EPI != EPI_BIAS_DROP_RES)
+                            load_bias<EPI>(p, g, n0 + (c + 1) * EPI_CHUNK, bpre);
+                    }
+                    if constexpr (EPI == EPI_BIAS_DROP_RES)
+                        load_bias<EPI>(p, g, n0 + c * EPI_CHUNK, curb);
                     ptx::tmem_ld_wait();
                     const int n = n0 + c * EPI_CHUNK;
                     if (n >= p.N || m0 >= p.M) continue;  // outside the tensor (warp-uniform)
                     float x[32], x2[32];
 #pragma unroll
                     for (int q = 0; q < 32; ++q) x[q] = __uint_as_float(v[q]);
-                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, cur);
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, cur, curb);
                     if (pace_clk && c > 0) pace_until(pace_t0 + c * pace_clk);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                     if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
@@ -1009,8 +1040,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     uint4 in[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                                    make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+                    uint4 bv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                   make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
                     load_in0<EPI>(p, part, in_row, m, n, in);
-                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, in);
+                    load_bias<EPI>(p, g, n, bv);
+                    epilogue_math<EPI>(p, g, part, in_row, m, n, x, x2, in, bv);
                     store_box(out1, out2, n, y0, x, x2, OUT_F32);
                     if constexpr (EPI == EPI_DGELU || EPI == EPI_DGELU_H) {
                         if (p.colsum_part) warp_column_sums(p, g, m0 + quarter * 32, m, n, lane, x);
