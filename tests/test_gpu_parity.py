@@ -187,6 +187,8 @@ def forced_tail_split():
     (128, 256, 1024, 2, 1),    # the tiny workload: every GEMM's tiles split
     (333, 264, 1032, 3, 1),    # ragged tails inside split tiles
     (512, 256, 1024, 4, 4),    # sequence-parallel chunks
+    (512, 512, 2048, 2, 1),    # 16 leftover tiles of 4 units
+    (333, 1024, 1536, 3, 1),   # 12 leftover tiles of 6 units
 ])
 def test_tail_split_full(forced_tail_split, T, h, f, t, chunks):
     _run_full(custom(T, h, f, t, sigma_w=0.05, seq_chunks=chunks), seed=12)
