@@ -2,8 +2,8 @@
 //
 // CTA = 256 threads over a 64-column strip: thread (slot, vec) reads the
 // 16-byte vector of 8 bf16 at columns vec*8.. of rows slot, slot+32, ...
-// (each warp covers four full 128-byte rows per load, coalesced), keeps 8
-// fp32 partial sums in registers, and the 32 row slots are then combined in
+// (each warp covers four full 128-byte rows per load, coalesced; eight loads
+// in flight per thread), keeps 8 fp32 partial sums in registers, and the 32 row slots are then combined in
 // a fixed order through shared memory.  With row splits, a second kernel
 // adds the per-split partial sums in split order.  No atomics, so the result
 // is bitwise reproducible.
@@ -22,6 +22,32 @@ __device__ __forceinline__ void add_bf16x8(const uint4& u, float (&acc)[8]) {
     }
 }
 
+// Moves (part, local row) d rows on, parts of rpp rows each.
+__device__ __forceinline__ void step_row(int& part, long long& lr, long long d, long long rpp) {
+    lr += d;
+    while (lr >= rpp) {
+        lr -= rpp;
+        ++part;
+    }
+}
+
+// p.src[i] by selects (indexing the parameter array with a run-time index
+// makes the compiler copy the whole parameter block to local memory per thread).
+__device__ __forceinline__ const void* part_src(const ColsumParams& p, int i) {
+    const void* s = p.src[0];
+#pragma unroll
+    for (int k = 1; k < CS_MAX_PARTS; ++k) s = i == k ? p.src[k] : s;
+    return s;
+}
+
+// The 16-byte vector at columns col.. of the row d rows after (part, lr).
+__device__ __forceinline__ uint4 load_row(const ColsumParams& p, int part, long long lr,
+                                          long long d, long long rpp, int col) {
+    step_row(part, lr, d, rpp);
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(part_src(p, part));
+    return __ldg(reinterpret_cast<const uint4*>(src + lr * p.ncols + col));
+}
+
 __global__ void __launch_bounds__(CS_THREADS) colsum_kernel(const ColsumParams p) {
     __shared__ float red[32][CS_COLS + 1];
     const int vec = threadIdx.x & 7;
@@ -38,34 +64,31 @@ __global__ void __launch_bounds__(CS_THREADS) colsum_kernel(const ColsumParams p
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
     if (col < p.ncols) {
+        // part and local row of this thread's row, stepped without a division
+        const long long rpp = p.mode == CS_ROWS_CONCAT ? p.rows_per_part : total_rows + 1;
         long long r = r0 + slot;
-        // four independent loads in flight per thread
+        int part = p.mode == CS_ROWS_CONCAT ? static_cast<int>(r / rpp) : grp;
+        long long lr = p.mode == CS_ROWS_CONCAT ? r - part * rpp : r;
+        // eight, then four independent loads in flight per thread, added in row order
+        for (; r + 224 < r1; r += 256) {
+            uint4 u[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = load_row(p, part, lr, 32 * q, rpp, col);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) add_bf16x8(u[q], acc);
+            step_row(part, lr, 256, rpp);
+        }
         for (; r + 96 < r1; r += 128) {
             uint4 u[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const long long rr = r + 32 * q;
-                int part = grp;
-                long long lr = rr;
-                if (p.mode == CS_ROWS_CONCAT) {
-                    part = static_cast<int>(rr / p.rows_per_part);
-                    lr = rr - part * p.rows_per_part;
-                }
-                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.src[part]);
-                u[q] = __ldg(reinterpret_cast<const uint4*>(src + lr * p.ncols + col));
-            }
+            for (int q = 0; q < 4; ++q) u[q] = load_row(p, part, lr, 32 * q, rpp, col);
 #pragma unroll
             for (int q = 0; q < 4; ++q) add_bf16x8(u[q], acc);
+            step_row(part, lr, 128, rpp);
         }
         for (; r < r1; r += 32) {
-            int part = grp;
-            long long lr = r;
-            if (p.mode == CS_ROWS_CONCAT) {
-                part = static_cast<int>(r / p.rows_per_part);
-                lr = r - part * p.rows_per_part;
-            }
-            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.src[part]);
-            add_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + lr * p.ncols + col)), acc);
+            add_bf16x8(load_row(p, part, lr, 0, rpp, col), acc);
+            step_row(part, lr, 32, rpp);
         }
     }
 #pragma unroll
@@ -145,10 +168,10 @@ dim3 colsum_plan(ColsumParams& p, int sm_count) {
     const long long total_rows =
         p.mode == CS_ROWS_CONCAT ? p.rows_per_part * p.nparts : p.rows_per_part;
     const long long base = static_cast<long long>(strips) * groups;
-    // many short CTAs (about sixteen per SM, at least 128 rows each), so the
-    // last of them to start ends soon after the rest
-    long long splits = (16LL * sm_count + base - 1) / base;
-    const long long max_by_rows = total_rows / 128 > 0 ? total_rows / 128 : 1;
+    // about four CTAs per SM (one wave), at least 256 rows (eight per thread)
+    // each, so every thread keeps eight loads in flight
+    long long splits = (4LL * sm_count + base - 1) / base;
+    const long long max_by_rows = total_rows / 256 > 0 ? total_rows / 256 : 1;
     if (splits > max_by_rows) splits = max_by_rows;
     if (splits > CS_MAX_SPLITS) splits = CS_MAX_SPLITS;
     if (splits < 1) splits = 1;

@@ -1,8 +1,9 @@
 // layernorm.cu -- LayerNorm forward/backward and dropout backward of the
-// sequence-parallel sublayer (see layernorm.cuh).  One CTA of 256 threads per
-// token row in the forward pass and in the dX pass of the backward; each
-// thread holds up to eight 8-element vectors of its row in registers, so every
-// input is read once and every output written once.  dgamma and dbeta come from a separate
+// sequence-parallel sublayer (see layernorm.cuh).  The forward pass runs one
+// warp per token row for rows of up to 4096 elements and one CTA of 256
+// threads per row beyond that, as does the dX pass of the backward; each
+// thread holds its vectors of the row in registers, so every input is read
+// once and every output written once.  dgamma and dbeta come from a separate
 // column-reduction pass over dXn and X.  The dropout backward reads the keep
 // bits the forward pass stored and sums dZ's columns (db2) as it goes.
 // Reductions run warp-shuffle then one warp over the partial sums, always in
@@ -64,6 +65,28 @@ __device__ __forceinline__ long long chunk_row(long long r, long long rows, int&
     return r - static_cast<long long>(j) * rows;
 }
 
+// Chunk and local row of a token row, moved along without a division (the
+// strip kernels step each thread's row by a fixed stride).
+struct ChunkPos {
+    int j;
+    long long lr;
+};
+
+__device__ __forceinline__ ChunkPos chunk_pos(long long r, long long rows) {
+    ChunkPos c;
+    c.lr = chunk_row(r, rows, c.j);
+    return c;
+}
+
+__device__ __forceinline__ ChunkPos chunk_advance(ChunkPos c, long long d, long long rows) {
+    c.lr += d;
+    while (c.lr >= rows) {
+        c.lr -= rows;
+        ++c.j;
+    }
+    return c;
+}
+
 // VEC = 8-element vectors per thread (h <= VEC * 8 * LN_THREADS): the row's
 // registers are sized to the row, so narrow rows keep more CTAs per SM.
 template <int VEC>
@@ -122,28 +145,92 @@ __global__ void __launch_bounds__(LN_THREADS) ln_forward_kernel(const LnForwardP
     }
 }
 
-// One 8-element vector of the dropout backward pass: dOut at (r, col) and the
-// keep bits of its 32-column word.
-__device__ __forceinline__ void dropout_load(const DropoutBackwardParams& p, long long r, int col,
-                                             uint4& u, uint32_t& word) {
+// One warp per token row, for rows of at most 32 * 8 * V elements (h a
+// multiple of 8): lane l holds the row's vectors l, l + 32, ...; the mean and
+// variance are warp-shuffle sums (no block barrier), so a warp starts its
+// row's loads as soon as it is scheduled and an SM keeps sixteen rows' loads
+// in flight.
+template <int V>
+__global__ void __launch_bounds__(LN_THREADS, 2) ln_forward_warp_kernel(const LnForwardParams p,
+                                                                        long long T) {
+    const int lane = threadIdx.x & 31;
+    const long long r = static_cast<long long>(blockIdx.x) * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    if (r >= T) return;
     int j;
-    const long long off = chunk_row(r, p.dout.rows, j) * p.h + col;
-    u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout.in[j]) + off));
+    const long long rr = chunk_row(r, p.x.rows, j);
+    const int h = p.h;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[j]) + rr * h;
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y[j]) + rr * h;
+    uint4 v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        const int c = (lane + 32 * i) * 8;
+        if (c < h) v[i] = *reinterpret_cast<const uint4*>(x + c);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        if ((lane + 32 * i) * 8 < h) {
+            float f[8];
+            unpack8(v[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s += f[k];
+        }
+    }
+    const float mean = warp_sum(s) / static_cast<float>(h);
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        if ((lane + 32 * i) * 8 < h) {
+            float f[8];
+            unpack8(v[i], f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q += (f[k] - mean) * (f[k] - mean);
+        }
+    }
+    const float var = warp_sum(q) / static_cast<float>(h);
+    const float rs = 1.0f / sqrtf(var + p.eps);
+    const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
+    const __nv_bfloat16* bt = static_cast<const __nv_bfloat16*>(p.beta);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        const int c = (lane + 32 * i) * 8;
+        if (c < h) {
+            float f[8], g[8], b[8], o[8];
+            unpack8(v[i], f);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gm + c)), g);
+            unpack8(__ldg(reinterpret_cast<const uint4*>(bt + c)), b);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = (f[k] - mean) * rs * g[k] + b[k];
+            *reinterpret_cast<uint4*>(y + c) = pack8(o);
+        }
+    }
+    if (lane == 0) {
+        p.mean[r] = mean;
+        p.rstd[r] = rs;
+    }
+}
+
+// One 8-element vector of the dropout backward pass: dOut at token row r
+// (chunk position c), columns col.., and the keep bits of its 32-column word.
+__device__ __forceinline__ void dropout_load(const DropoutBackwardParams& p, ChunkPos c,
+                                             long long r, int col, uint4& u, uint32_t& word) {
+    const long long off = c.lr * p.h + col;
+    u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout.in[c.j]) + off));
     word = __ldg(p.drop.mask + r * p.drop.mask_words + col / 32);
 }
 
 // dZ for that vector, stored; its bf16 values added to acc.
-__device__ __forceinline__ void dropout_apply(const DropoutBackwardParams& p, long long r, int col,
+__device__ __forceinline__ void dropout_apply(const DropoutBackwardParams& p, ChunkPos c, int col,
                                               const uint4& u, uint32_t word, float (&acc)[8]) {
-    int j;
-    const long long off = chunk_row(r, p.dout.rows, j) * p.h + col;
+    const long long off = c.lr * p.h + col;
     const uint32_t bits = word >> (col & 31);
     float f[8];
     unpack8(u, f);
 #pragma unroll
     for (int k = 0; k < 8; ++k) f[k] = ((bits >> k) & 1u) ? f[k] * p.drop.scale : 0.0f;
     const uint4 o = pack8(f);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dz[j]) + off) = o;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dz[c.j]) + off) = o;
     float g[8];
     unpack8(o, g);
 #pragma unroll
@@ -154,8 +241,8 @@ __device__ __forceinline__ void dropout_apply(const DropoutBackwardParams& p, lo
 // and the column sums of dZ (as rounded to bf16) per row split: CTA = a
 // 64-column strip x 32 row slots over the rows of split blockIdx.y; thread
 // (slot, vec) handles columns vec*8 .. vec*8+7 of rows slot, slot + 32, ...
-// (four rows' loads in flight), and the slots are added in order through
-// shared memory into part[split][col].
+// (four rows' loads in flight, added in row order), and the slots are added
+// in order through shared memory into part[split][col].
 __global__ void __launch_bounds__(LN_THREADS, 3) dropout_backward_kernel(const DropoutBackwardParams p,
                                                                       long long T) {
     constexpr int COLS = 64;
@@ -169,24 +256,26 @@ __global__ void __launch_bounds__(LN_THREADS, 3) dropout_backward_kernel(const D
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
     if (col < h) {
+        const long long rows = p.dout.rows;
         long long r = r0 + slot;
+        ChunkPos c = chunk_pos(r, rows);
         for (; r + 96 < r1; r += 128) {
-            uint4 u0, u1, u2, u3;
-            uint32_t w0, w1, w2, w3;
-            dropout_load(p, r, col, u0, w0);
-            dropout_load(p, r + 32, col, u1, w1);
-            dropout_load(p, r + 64, col, u2, w2);
-            dropout_load(p, r + 96, col, u3, w3);
-            dropout_apply(p, r, col, u0, w0, acc);
-            dropout_apply(p, r + 32, col, u1, w1, acc);
-            dropout_apply(p, r + 64, col, u2, w2, acc);
-            dropout_apply(p, r + 96, col, u3, w3, acc);
+            uint4 u[4];
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dropout_load(p, chunk_advance(c, 32 * q, rows), r + 32 * q, col, u[q], w[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dropout_apply(p, chunk_advance(c, 32 * q, rows), col, u[q], w[q], acc);
+            c = chunk_advance(c, 128, rows);
         }
         for (; r < r1; r += 32) {
             uint4 u;
             uint32_t w;
-            dropout_load(p, r, col, u, w);
-            dropout_apply(p, r, col, u, w, acc);
+            dropout_load(p, c, r, col, u, w);
+            dropout_apply(p, c, col, u, w, acc);
+            c = chunk_advance(c, 32, rows);
         }
     }
 #pragma unroll
@@ -289,9 +378,9 @@ __global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParam
 
 // dgamma / dbeta partial column sums: CTA = a 64-column strip x 32 row slots
 // over the rows of split blockIdx.y; thread (slot, vec) accumulates columns
-// vec*8 .. vec*8+7 of rows slot, slot + 32, ...; the slots are then added in
-// order through shared memory.  part[split][0][c] = sum dXn * xhat,
-// part[split][1][c] = sum dXn.
+// vec*8 .. vec*8+7 of rows slot, slot + 32, ... (four rows' loads in flight,
+// added in row order); the slots are then added in order through shared
+// memory.  part[split][0][c] = sum dXn * xhat, part[split][1][c] = sum dXn.
 __global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackwardParams p,
                                                                    long long T) {
     constexpr int COLS = 64;
@@ -304,21 +393,44 @@ __global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackw
     float ag[8], ab[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) ag[k] = ab[k] = 0.0f;
-    if (col < h) {
-        for (long long r = r0 + slot; r < r1; r += 32) {
-            int j;
-            const long long off = chunk_row(r, p.x.rows, j) * h + col;
-            float xf[8], df[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(
-                        static_cast<const __nv_bfloat16*>(p.x.in[j]) + off)), xf);
-            unpack8(__ldg(reinterpret_cast<const uint4*>(
-                        static_cast<const __nv_bfloat16*>(p.dxn[j]) + off)), df);
-            const float mean = __ldg(p.mean + r), rs = __ldg(p.rstd + r);
+    // row r's inputs, then its terms added to the sums
+    auto load = [&](ChunkPos c, long long r, uint4& xu, uint4& du, float& mean, float& rs) {
+        const long long off = c.lr * h + col;
+        xu = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x.in[c.j]) + off));
+        du = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dxn[c.j]) + off));
+        mean = __ldg(p.mean + r);
+        rs = __ldg(p.rstd + r);
+    };
+    auto add = [&](const uint4& xu, const uint4& du, float mean, float rs) {
+        float xf[8], df[8];
+        unpack8(xu, xf);
+        unpack8(du, df);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                ag[k] += df[k] * ((xf[k] - mean) * rs);
-                ab[k] += df[k];
-            }
+        for (int k = 0; k < 8; ++k) {
+            ag[k] += df[k] * ((xf[k] - mean) * rs);
+            ab[k] += df[k];
+        }
+    };
+    if (col < h) {
+        const long long rows = p.x.rows;
+        long long r = r0 + slot;
+        ChunkPos c = chunk_pos(r, rows);
+        for (; r + 96 < r1; r += 128) {
+            uint4 xu[4], du[4];
+            float mn[4], rs[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                load(chunk_advance(c, 32 * q, rows), r + 32 * q, xu[q], du[q], mn[q], rs[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) add(xu[q], du[q], mn[q], rs[q]);
+            c = chunk_advance(c, 128, rows);
+        }
+        for (; r < r1; r += 32) {
+            uint4 xu, du;
+            float mn, rs;
+            load(c, r, xu, du, mn, rs);
+            add(xu, du, mn, rs);
+            c = chunk_advance(c, 32, rows);
         }
     }
 #pragma unroll
@@ -348,6 +460,18 @@ int ln_vec(int h) {
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st) {
     if (T <= 0) return cudaSuccess;
+    if (p.h % 8 == 0 && p.h <= LN_WARP_MAX_H) {
+        // rows of up to 4096 elements: one warp per row
+        constexpr int RPB = LN_THREADS / 32;
+        const unsigned blocks = static_cast<unsigned>((T + RPB - 1) / RPB);
+        if (p.h <= 1024)
+            ln_forward_warp_kernel<4><<<blocks, LN_THREADS, 0, st>>>(p, T);
+        else if (p.h <= 2048)
+            ln_forward_warp_kernel<8><<<blocks, LN_THREADS, 0, st>>>(p, T);
+        else
+            ln_forward_warp_kernel<16><<<blocks, LN_THREADS, 0, st>>>(p, T);
+        return cudaGetLastError();
+    }
     const unsigned grid = static_cast<unsigned>(T);
     switch (ln_vec(p.h)) {
         case 1: ln_forward_kernel<1><<<grid, LN_THREADS, 0, st>>>(p); break;

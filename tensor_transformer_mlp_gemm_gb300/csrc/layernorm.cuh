@@ -23,6 +23,7 @@ namespace tpmlp {
 constexpr int LN_THREADS = 256;
 constexpr int LN_MAX_VEC = 8;                          // 8-element vectors per thread
 constexpr int LN_MAX_H = LN_THREADS * LN_MAX_VEC * 8;  // 16384
+constexpr int LN_WARP_MAX_H = 32 * 16 * 8;             // rows the one-warp forward kernel takes
 constexpr int LN_MAX_CHUNKS = 8;
 
 struct LnChunks {
