@@ -450,6 +450,11 @@ enum {
     TPMLP_KERNEL_KINDS = 14
 };
 tpmlp_status tpmlp_profile_begin(int capacity);
+/* The same, with event pairs only around the launches of the kernel kinds
+ * whose bits are set in `kinds` (bit k = kind k): timing one kind costs the
+ * others no event records.  TPMLP_ERR_INVALID_ARG for capacity <= 0, kinds
+ * == 0 or a bit at or above TPMLP_KERNEL_KINDS. */
+tpmlp_status tpmlp_profile_begin_kinds(int capacity, uint32_t kinds);
 int tpmlp_profile_end(double* ms, int* launches, int nkinds);
 const char* tpmlp_kernel_name(int kind);
 

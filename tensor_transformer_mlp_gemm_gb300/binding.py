@@ -33,7 +33,8 @@ KERNEL_KINDS = 14
 EXPORTED = (
     "tpmlp_workspace_bytes", "tpmlp_workspace_layout", "tpmlp_forward", "tpmlp_backward",
     "tpmlp_status_string", "tpmlp_sync_check", "tpmlp_set_wait_timeout_ns",
-    "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_end",
+    "tpmlp_selftest_stalled_gemm", "tpmlp_profile_begin", "tpmlp_profile_begin_kinds",
+    "tpmlp_profile_end",
     "tpmlp_kernel_name", "tpmlp_column_sums_noalloc", "tpmlp_set_split_min_kblocks",
     "tpmlp_recompute_workspace_bytes", "tpmlp_forward_recompute", "tpmlp_backward_recompute",
     "tpmlp_linear_workspace_bytes", "tpmlp_column_linear_forward", "tpmlp_column_linear_backward",
@@ -112,6 +113,8 @@ _lib.tpmlp_selftest_stalled_gemm.restype = ctypes.c_int
 _lib.tpmlp_selftest_stalled_gemm.argtypes = [_vp, _vp, _vp, ctypes.c_uint64, _vp]
 _lib.tpmlp_profile_begin.restype = ctypes.c_int
 _lib.tpmlp_profile_begin.argtypes = [ctypes.c_int]
+_lib.tpmlp_profile_begin_kinds.restype = ctypes.c_int
+_lib.tpmlp_profile_begin_kinds.argtypes = [ctypes.c_int, ctypes.c_uint32]
 _lib.tpmlp_profile_end.restype = ctypes.c_int
 _lib.tpmlp_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                    ctypes.c_int]
@@ -287,6 +290,15 @@ def tpmlp_selftest_stalled_gemm(a, b, c, timeout_ns: int, stream=None) -> int:
 
 def tpmlp_profile_begin(capacity: int) -> None:
     _check(_lib.tpmlp_profile_begin(int(capacity)), "tpmlp_profile_begin")
+
+
+def tpmlp_profile_begin_kinds(capacity: int, kinds) -> None:
+    """Profile only the named kernel kinds (names as tpmlp_kernel_name)."""
+    names = [tpmlp_kernel_name(k) for k in range(KERNEL_KINDS)]
+    mask = 0
+    for k in kinds:
+        mask |= 1 << names.index(k)
+    _check(_lib.tpmlp_profile_begin_kinds(int(capacity), mask), "tpmlp_profile_begin_kinds")
 
 
 def tpmlp_profile_end() -> tuple[dict, dict]:

@@ -66,12 +66,14 @@ EncodeTiledFn g_encode = nullptr;
 // ---- profiling ------------------------------------------------------------------
 std::mutex g_prof_mu;
 bool g_prof_on = false;
+uint32_t g_prof_kinds = ~0u;  // kinds that get event pairs while profiling
 std::vector<ProfRec> g_prof_pool;
 size_t g_prof_used = 0;
 
 ProfRec* prof_next(int kind, int kernels) {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on || g_prof_used >= g_prof_pool.size()) return nullptr;
+    if (kind < 0 || kind >= 32 || !((g_prof_kinds >> kind) & 1u)) return nullptr;
     ProfRec* r = &g_prof_pool[g_prof_used++];
     r->kind = kind;
     r->kernels = kernels;
@@ -854,9 +856,11 @@ TPMLP_API tpmlp_status tpmlp_selftest_stalled_gemm(const void* a, const void* b,
     return tpmlp_sync_check(stream);
 }
 
-TPMLP_API tpmlp_status tpmlp_profile_begin(int capacity) {
-    if (capacity <= 0) return TPMLP_ERR_INVALID_ARG;
+TPMLP_API tpmlp_status tpmlp_profile_begin_kinds(int capacity, uint32_t kinds) {
+    if (capacity <= 0 || kinds == 0 || (kinds >> TPMLP_KERNEL_KINDS) != 0)
+        return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_kinds = kinds;
     for (auto& r : g_prof_pool) {
         cudaEventDestroy(r.a);
         cudaEventDestroy(r.b);
@@ -869,6 +873,10 @@ TPMLP_API tpmlp_status tpmlp_profile_begin(int capacity) {
     g_prof_used = 0;
     g_prof_on = true;
     return TPMLP_OK;
+}
+
+TPMLP_API tpmlp_status tpmlp_profile_begin(int capacity) {
+    return tpmlp_profile_begin_kinds(capacity, (1u << TPMLP_KERNEL_KINDS) - 1u);
 }
 
 TPMLP_API int tpmlp_profile_end(double* ms, int* launches, int nkinds) {

@@ -232,6 +232,9 @@ def test_set_timeout_and_profile_args(binding):
     assert lib.tpmlp_set_wide_tiles(3) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_set_wide_tiles(-1) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_profile_begin(0) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_profile_begin_kinds(0, 1) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_profile_begin_kinds(16, 0) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_profile_begin_kinds(16, 1 << binding.KERNEL_KINDS) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_profile_end(None, None, 0) == -1  # not profiling
 
 
