@@ -128,6 +128,29 @@ def test_gpt_175b_sampled():
     assert torch.equal(blk.dA[3], dA0)
 
 
+FULL_ORACLE = os.environ.get("TPMLP_FULL_ORACLE") == "1"
+
+
+@pytest.mark.skipif(not FULL_ORACLE, reason="every element of the full-size layers against the "
+                    "fp64 oracle takes about four minutes of host time per layer; "
+                    "TPMLP_FULL_ORACLE=1 runs it")
+@pytest.mark.parametrize("name", ["gpt_175b", "sp_h4096"])
+def test_full_size_every_element(name):
+    """The 175B-class and sequence-parallel layers, every output and gradient
+    element (Y, H, dY, Z, dX, dA, dB, db1, db2) against the full fp64 oracle."""
+    w = WORKLOADS[name]
+    inputs = make_inputs(w, 0)
+    blk = _block(w, inputs)
+    blk.step()
+    torch.cuda.synchronize()
+    ref = _oracle_full(w, inputs)
+    rep = {}
+    compare_full(blk, ref, rep)
+    for k, m in rep.items():
+        print(f"{name} {k}: rel_fro {m['rel_fro']:.3e} max_abs {m['max_abs']:.3e} "
+              f"bound {m['bound']:.3e}")
+
+
 def test_sequence_parallel_sampled_and_equal_to_plain():
     w = WORKLOADS["sp_h4096"]
     inputs = make_inputs(w, 0)
