@@ -3,10 +3,10 @@
 // CTA = 256 threads over a 64-column strip: thread (slot, vec) reads the
 // 16-byte vector of 8 bf16 at columns vec*8.. of rows slot, slot+32, ...
 // (each warp covers four full 128-byte rows per load, coalesced; eight loads
-// in flight per thread), keeps 8 fp32 partial sums in registers, and the 32 row slots are then combined in
-// a fixed order through shared memory.  With row splits, a second kernel
-// adds the per-split partial sums in split order.  No atomics, so the result
-// is bitwise reproducible.
+// in flight per thread), keeps 8 fp32 partial sums in registers, and the 32
+// row slots are then combined in a fixed order through shared memory.  With
+// row splits, a second kernel adds the per-split partial sums in split order.
+// No atomics, so the result is bitwise reproducible.
 #include <cuda_bf16.h>
 
 #include "colsum.cuh"
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(CS_THREADS) colsum_kernel(const ColsumParams p
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 
-    if (col < p.ncols) {
+    if (col < p.ncols && r0 + slot < r1) {
         // part and local row of this thread's row, stepped without a division
         const long long rpp = p.mode == CS_ROWS_CONCAT ? p.rows_per_part : total_rows + 1;
         long long r = r0 + slot;

@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(LN_THREADS, 2) ln_forward_warp_kernel(const Ln
 __device__ __forceinline__ void dropout_load(const DropoutBackwardParams& p, ChunkPos c,
                                              long long r, int col, uint4& u, uint32_t& word) {
     const long long off = c.lr * p.h + col;
-    u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout.in[c.j]) + off));
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.dout.in[c.j]);
+    u = __ldg(reinterpret_cast<const uint4*>(src + off));
     word = __ldg(p.drop.mask + r * p.drop.mask_words + col / 32);
 }
 
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(LN_THREADS, 3) dropout_backward_kernel(const D
     float acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-    if (col < h) {
+    if (col < h && r0 + slot < r1) {
         const long long rows = p.dout.rows;
         long long r = r0 + slot;
         ChunkPos c = chunk_pos(r, rows);
@@ -396,8 +397,10 @@ __global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackw
     // row r's inputs, then its terms added to the sums
     auto load = [&](ChunkPos c, long long r, uint4& xu, uint4& du, float& mean, float& rs) {
         const long long off = c.lr * h + col;
-        xu = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.x.in[c.j]) + off));
-        du = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dxn[c.j]) + off));
+        const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(p.x.in[c.j]);
+        const __nv_bfloat16* ds = static_cast<const __nv_bfloat16*>(p.dxn[c.j]);
+        xu = __ldg(reinterpret_cast<const uint4*>(xs + off));
+        du = __ldg(reinterpret_cast<const uint4*>(ds + off));
         mean = __ldg(p.mean + r);
         rs = __ldg(p.rstd + r);
     };
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_param_grad_kernel(const LnBackw
             ab[k] += df[k];
         }
     };
-    if (col < h) {
+    if (col < h && r0 + slot < r1) {
         const long long rows = p.x.rows;
         long long r = r0 + slot;
         ChunkPos c = chunk_pos(r, rows);
