@@ -93,9 +93,10 @@ def parse_args():
                     help="tail-split depth threshold of the GEMMs (0 = off; library default 128)")
     ap.add_argument("--head-prefetch", type=int, default=None,
                     help="K steps of the next tile the GEMMs prefetch into L2 (library default)")
-    ap.add_argument("--wide-tiles", type=int, default=None, choices=[0, 1, 2],
-                    help="GEMM tile width: 0 = 256-wide (library default), 1 = 512-wide where "
-                         "the waves fill as well, 2 = 512-wide wherever allowed")
+    ap.add_argument("--wide-tiles", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="GEMM tile width: 0 = 256-wide, 1 = 512-wide where the waves fill as "
+                         "well, 2 = 512-wide wherever allowed, 3 = 512-wide for GEMMs of at least "
+                         "256 K steps (library default)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph (the per-kernel "
                          "times then come from eager steps run after the timed region)")

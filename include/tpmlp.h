@@ -340,12 +340,14 @@ tpmlp_status tpmlp_set_head_prefetch(int kblocks);
  * accumulators in tensor memory: a tile's epilogue runs under the next
  * tile's MMAs) or 256 x 512 tiles (one accumulator in two halves, K steps in
  * three phases so each half drains under MMAs on the other), which move a
- * quarter fewer operand bytes from L2 per FLOP.  mode 0 (default) always 256,
- * 1 picks 512 where its tiles fill the GPU's waves at least as well as
- * 256-wide ones, 2 always 512.  0, 1 or 2, else TPMLP_ERR_INVALID_ARG.  Half 0
- * of a wide tile sums K in the narrow tile's order (bitwise equal columns);
- * half 1 starts its sum further along K (equal within rounding).  Affects
- * launches enqueued after the call. */
+ * quarter fewer operand bytes from L2 per FLOP.  mode 0 always 256; 1 picks
+ * 512 where its tiles fill the GPU's waves at least as well as 256-wide ones;
+ * 2 always 512; 3 (default) picks 512 for GEMMs of at least 256 K steps of 64
+ * (summed over the row-parallel shards), where the one-half phases are a
+ * small share and the lower operand traffic lowers the power drawn.  0 to 3,
+ * else TPMLP_ERR_INVALID_ARG.  Half 0 of a wide tile sums K in the narrow
+ * tile's order (bitwise equal columns); half 1 starts its sum further along K
+ * (equal within rounding).  Affects launches enqueued after the call. */
 tpmlp_status tpmlp_set_wide_tiles(int mode);
 
 /* TMA tensor-map cache.  Every call encodes one tensor map per operand shard,

@@ -257,9 +257,13 @@ def tpmlp_set_head_prefetch(kblocks: int) -> None:
     _check(_lib.tpmlp_set_head_prefetch(int(kblocks)), "tpmlp_set_head_prefetch")
 
 
+WIDE_TILES_DEFAULT = 3
+
+
 def tpmlp_set_wide_tiles(mode: int) -> None:
-    """0 (default): 256-wide GEMM tiles; 1: 512-wide where they fill the waves as
-    well; 2: 512-wide wherever allowed."""
+    """0: 256-wide GEMM tiles; 1: 512-wide where they fill the waves as well;
+    2: 512-wide wherever allowed; 3 (default): 512-wide for GEMMs of at least
+    256 K steps."""
     _check(_lib.tpmlp_set_wide_tiles(int(mode)), "tpmlp_set_wide_tiles")
 
 

@@ -77,9 +77,10 @@ tpmlp_status check_ptr(const void* p);
 // K segments, with the device's error word and the current wait limit.
 void base_params(GemmParams& p, const DeviceInfo& dev, int M, int N, int K, int groups,
                  int ksegs);
-// Chooses the tile width of a GEMM with a bf16 output (wide tiles where they
-// fill the GPU's waves as well as narrow ones; see tpmlp_set_wide_tiles) and
-// sets tn, ntiles and total_tiles.  The B maps are encoded after this.
+// Chooses the tile width of a GEMM with a bf16 output by the policy of
+// tpmlp_set_wide_tiles (by default wide tiles for GEMMs of at least
+// WIDE_MIN_KSTEPS K steps; K and ksegs must be set) and sets tn, ntiles and
+// total_tiles.  The B maps are encoded after this.
 void choose_tile_width(GemmParams& p, const DeviceInfo& dev);
 // Points the tail split at its workspace buffers (split_part_bytes() and
 // split_cnt_bytes() long).

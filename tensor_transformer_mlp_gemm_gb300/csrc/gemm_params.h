@@ -19,6 +19,10 @@ constexpr int BM = 128;            // tile rows per CTA (TMEM lanes)
 constexpr int CLUSTER_M = 2 * BM;  // tile rows per CTA pair
 constexpr int BN = 256;       // narrow tile columns (TMEM columns per accumulator)
 constexpr int BN_WIDE = 512;  // wide tile columns (the whole of TMEM)
+// tile-width policy of the bf16-output GEMMs (tpmlp_set_wide_tiles): the
+// default takes wide tiles for GEMMs of at least WIDE_MIN_KSTEPS K steps
+constexpr int WIDE_TILES_DEEP_K = 3;
+constexpr int WIDE_MIN_KSTEPS = 256;
 constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
 constexpr int STAGES = 6;
 constexpr int A_STAGE_BYTES = BM * BK * 2;

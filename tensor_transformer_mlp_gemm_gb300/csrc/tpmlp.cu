@@ -55,7 +55,7 @@ DeviceInfo g_dev[kMaxDevices];
 unsigned long long g_timeout_ns = 2000000000ULL;
 int g_split_min_kblocks = DEFAULT_SPLIT_MIN_KBLOCKS;
 int g_head_prefetch = 0;
-int g_wide_tiles = 0;
+int g_wide_tiles = WIDE_TILES_DEEP_K;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -235,8 +235,17 @@ static double tile_waves(const GemmParams& p, int tn, int pairs) {
 
 void choose_tile_width(GemmParams& p, const DeviceInfo& dev) {
     int tn = BN;
+    const int nk = ((p.K + BK - 1) / BK) * p.ksegs;
     if (g_wide_tiles == 2) {
         tn = BN_WIDE;
+    } else if (g_wide_tiles == WIDE_TILES_DEEP_K) {
+        // deep K: the one-half phases are a small share of a tile's K steps,
+        // and the quarter fewer operand bytes per FLOP lower the power the
+        // GEMM draws, which under the power cap raises the clock of every
+        // kernel of the step (measured: the 175B-class layer's row and dX
+        // GEMMs, 768 K steps, +1.2 % per step; 16384 x 4096, 256 K steps,
+        // +1.9 %; 128 K steps, -0.3 to -0.9 %)
+        if (nk >= WIDE_MIN_KSTEPS) tn = BN_WIDE;
     } else if (g_wide_tiles == 1) {
         // the same work in no more time: waves x tile width (a wide tile is
         // twice a narrow one's work); ties go to the wide tile, which moves a
@@ -622,7 +631,7 @@ TPMLP_API tpmlp_status tpmlp_set_head_prefetch(int kblocks) {
 }
 
 TPMLP_API tpmlp_status tpmlp_set_wide_tiles(int mode) {
-    if (mode < 0 || mode > 2) return TPMLP_ERR_INVALID_ARG;
+    if (mode < 0 || mode > WIDE_TILES_DEEP_K) return TPMLP_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(g_mu);
     g_wide_tiles = mode;
     return TPMLP_OK;

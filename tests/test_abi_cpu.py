@@ -229,7 +229,7 @@ def test_set_timeout_and_profile_args(binding):
     assert lib.tpmlp_set_split_min_kblocks(-1) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_set_head_prefetch(-1) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_set_head_prefetch(65) == binding.TPMLP_ERR_INVALID_ARG
-    assert lib.tpmlp_set_wide_tiles(3) == binding.TPMLP_ERR_INVALID_ARG
+    assert lib.tpmlp_set_wide_tiles(4) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_set_wide_tiles(-1) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_profile_begin(0) == binding.TPMLP_ERR_INVALID_ARG
     assert lib.tpmlp_profile_begin_kinds(0, 1) == binding.TPMLP_ERR_INVALID_ARG

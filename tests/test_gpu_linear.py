@@ -282,4 +282,4 @@ def test_wide_tiles_full(split, T, din, dout, t, chunks):
         else:
             _run_full(custom_linear(T, dout, din, t, split, sigma_w=0.05, seq_chunks=chunks), seed=5)
     finally:
-        binding.tpmlp_set_wide_tiles(0)
+        binding.tpmlp_set_wide_tiles(binding.WIDE_TILES_DEFAULT)

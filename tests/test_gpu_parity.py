@@ -309,7 +309,7 @@ def wide_tiles_forced():
     from tensor_transformer_mlp_gemm_gb300 import binding
     binding.tpmlp_set_wide_tiles(2)
     yield
-    binding.tpmlp_set_wide_tiles(0)
+    binding.tpmlp_set_wide_tiles(binding.WIDE_TILES_DEFAULT)
 
 
 @pytest.mark.parametrize("T,h,f,t,chunks", [
@@ -349,7 +349,7 @@ def test_wide_tiles_match_narrow():
         wide = _block(w, inputs)
         wide.step()
     finally:
-        binding.tpmlp_set_wide_tiles(0)
+        binding.tpmlp_set_wide_tiles(binding.WIDE_TILES_DEFAULT)
         binding.tpmlp_set_split_min_kblocks(128)
     torch.cuda.synchronize()
     sn, sw = narrow.saved(), wide.saved()

@@ -107,7 +107,7 @@ def test_sp_layer_wide_tiles_full(T, h, f, t, chunks, p):
     try:
         _run_full(custom(T, h, f, t, seq_chunks=chunks), p, seed=6)
     finally:
-        binding.tpmlp_set_wide_tiles(0)
+        binding.tpmlp_set_wide_tiles(binding.WIDE_TILES_DEFAULT)
 
 
 def test_sp_layer_deterministic_and_seeded():
