@@ -303,6 +303,26 @@ def test_tensor_map_cache_hits_on_repeat_and_misses_on_new_buffers():
     _assert_bitwise(b.Z + b.dA, first, "new buffers")
 
 
+def test_profile_only_the_chosen_kinds():
+    """tpmlp_profile_begin_kinds times the chosen kernel kinds only: one step of
+    the block records launches of those kinds and none of the others."""
+    from tensor_transformer_mlp_gemm_gb300 import binding
+    w = custom(512, 256, 1024, 2)
+    b = _block(w, make_inputs(w, 20))
+    b.step()
+    torch.cuda.synchronize()
+    binding.tpmlp_profile_begin_kinds(64, ["column_fwd", "wgrad_a"])
+    b.step()
+    ms, count = binding.tpmlp_profile_end()
+    assert count["column_fwd"] == 1 and count["wgrad_a"] == 1
+    assert ms["column_fwd"] > 0 and ms["wgrad_a"] > 0
+    assert all(count[k] == 0 for k in count if k not in ("column_fwd", "wgrad_a"))
+    binding.tpmlp_profile_begin(64)
+    b.step()
+    _, every = binding.tpmlp_profile_end()
+    assert every["row_fwd"] == 1 and every["dgrad_h"] == 1 and every["bias_grad"] >= 1
+
+
 @pytest.fixture
 def wide_tiles_forced():
     """Run every bf16-output GEMM with 256 x 512 pair tiles, whatever the size."""
