@@ -754,7 +754,8 @@ class SpRunner(MlpRunner):
         # bias-gradient kernels: only db1's finish here (db2 comes out of the dropout pass)
         self.colsum_bytes = ((T + 31) // 32) * f * 4 + f * 4
         # LayerNorm forward reads X, writes LN(X); backward reads X, dLN(X), dOut and writes
-        # dX (the dgamma / dbeta pass re-reads X and dLN(X): not counted, algorithmic bytes only)
+        # dX; dgamma and dbeta come out of the same pass (h <= 4096; wider rows re-read X and
+        # dLN(X) in a second pass, not counted: algorithmic bytes only)
         self.ln_fwd_bytes = 2 * T * h * 2
         self.ln_bwd_bytes = 4 * T * h * 2
         # dropout backward reads dOut and the mask's bits, writes dZ (and db2 from it)

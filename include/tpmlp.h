@@ -446,7 +446,7 @@ enum {
     TPMLP_KERNEL_LINEAR_DGRAD = 8,  /* linear layers: dX = sum_i dY_i.W_i^T, dX_i = dZ.W_i^T */
     TPMLP_KERNEL_LINEAR_WGRAD = 9,  /* linear layers: dW_i */
     TPMLP_KERNEL_LAYERNORM_FWD = 10,  /* sequence-parallel sublayer: LN(X) and row statistics */
-    TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (4 launches) */
+    TPMLP_KERNEL_LAYERNORM_BWD = 11,  /* sequence-parallel sublayer: dX, dgamma, dbeta (2 launches; 3 for h > 4096) */
     TPMLP_KERNEL_DROPOUT_BWD = 12,    /* sequence-parallel sublayer: dZ from dOut and the mask, db2 (2 launches) */
     TPMLP_KERNEL_SP_COPY = 13,        /* tpmlp_sp_gather / tpmlp_sp_scatter */
     TPMLP_KERNEL_KINDS = 14

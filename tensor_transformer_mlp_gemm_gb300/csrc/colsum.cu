@@ -121,10 +121,13 @@ __global__ void colsum_finish_kernel(const float* __restrict__ partial, int spli
 
 // CTA = 16 column quads (64 columns) x 16 row lanes; lane r sums rows r,
 // r + 16, ... of its four columns with 16-byte loads, then the 16 lanes are
-// combined in a fixed order.
+// combined in a fixed order.  Column c < split goes to out0[c], the others to
+// out1[c - split].
 __global__ void __launch_bounds__(256) colsum_f32_kernel(const float* __restrict__ part,
                                                          long long rows, long long ld,
-                                                         long long ncols, float* __restrict__ out) {
+                                                         long long ncols, long long split,
+                                                         float* __restrict__ out0,
+                                                         float* __restrict__ out1) {
     __shared__ float4 red[16][16];
     const int quad = threadIdx.x & 15;
     const int lane_r = threadIdx.x >> 4;
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(256) colsum_f32_kernel(const float* __restrict
             s.z += v.z;
             s.w += v.w;
         }
-        *reinterpret_cast<float4*>(out + c) = s;
+        *reinterpret_cast<float4*>(c < split ? out0 + c : out1 + (c - split)) = s;
     }
 }
 
@@ -158,7 +161,16 @@ cudaError_t launch_colsum_f32(const float* part, long long rows, long long ld, l
                               float* out, cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>((ncols + 63) / 64);
     if (blocks == 0) return cudaSuccess;
-    colsum_f32_kernel<<<blocks, 256, 0, stream>>>(part, rows, ld, ncols, out);
+    colsum_f32_kernel<<<blocks, 256, 0, stream>>>(part, rows, ld, ncols, ncols, out, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_f32_pair(const float* part, long long rows, long long ld,
+                                   long long ncols, float* out0, float* out1,
+                                   cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((2 * ncols + 63) / 64);
+    if (blocks == 0) return cudaSuccess;
+    colsum_f32_kernel<<<blocks, 256, 0, stream>>>(part, rows, ld, 2 * ncols, ncols, out0, out1);
     return cudaGetLastError();
 }
 

@@ -46,5 +46,10 @@ cudaError_t launch_colsum(const ColsumParams& p, dim3 grid, cudaStream_t stream,
 // and ld multiples of 4, part and out 16-byte aligned.
 cudaError_t launch_colsum_f32(const float* part, long long rows, long long ld, long long ncols,
                               float* out, cudaStream_t stream);
+// The same over the first 2 * ncols columns in one launch: out0[c] for c < ncols,
+// out1[c] for column ncols + c (two row-interleaved sums, e.g. [rows][2][ncols]).
+cudaError_t launch_colsum_f32_pair(const float* part, long long rows, long long ld,
+                                   long long ncols, float* out0, float* out1,
+                                   cudaStream_t stream);
 
 }  // namespace tpmlp

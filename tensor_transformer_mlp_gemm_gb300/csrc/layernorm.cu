@@ -317,6 +317,29 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
     return make_float2(red[2 * W], red[2 * W + 1]);
 }
 
+// Sum of two values over the CTA with one barrier: red holds two buffers of
+// 2 x (LN_THREADS / 32) floats, used by alternate calls (buf = 0, 1, 0, ...),
+// so a call's writes cannot meet the previous call's reads; every thread adds
+// the warps' partial sums in the same order.
+__device__ __forceinline__ float2 block_sum2_1bar(float a, float b, float* red, int buf) {
+    constexpr int W = LN_THREADS / 32;
+    a = warp_sum(a);
+    b = warp_sum(b);
+    float* rb = red + buf * 2 * W;
+    if ((threadIdx.x & 31) == 0) {
+        rb[threadIdx.x >> 5] = a;
+        rb[W + (threadIdx.x >> 5)] = b;
+    }
+    __syncthreads();
+    float ta = rb[0], tb = rb[W];
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+        ta += rb[w];
+        tb += rb[W + w];
+    }
+    return make_float2(ta, tb);
+}
+
 // dX of one token row per CTA:
 //   dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dres,  g = dXn * gamma
 template <int VEC>
@@ -373,6 +396,121 @@ __global__ void __launch_bounds__(LN_THREADS) ln_dx_kernel(const LnBackwardParam
             for (int k = 0; k < 8; ++k)
                 o[k] = rs * (df[k] * gf[k] - mg - (xf[k] - mean) * rs * mgx) + rf[k];
             *reinterpret_cast<uint4*>(dx + c) = pack8(o);
+        }
+    }
+}
+
+// Rows of at most LN_WARP_MAX_H elements: dX and the dgamma / dbeta partial
+// sums in one pass.  CTA b walks token rows [b * rows_per_block, ...) in
+// order with the next row's X, dXn and residual gradient loads in flight;
+// each thread keeps gamma and the partial sums of its columns in registers,
+// so X and dXn are read once:
+// part[b][0][c] = sum dXn * xhat, part[b][1][c] = sum dXn, added over the
+// blocks in a fixed order by the finishing kernels.
+template <int VEC>
+__global__ void __launch_bounds__(LN_THREADS, 2) ln_backward_fused_kernel(const LnBackwardParams p,
+                                                                          long long T) {
+    __shared__ float red[4 * (LN_THREADS / 32)];
+    const int h = p.h;
+    const long long rows = p.x.rows;
+    const long long r0 = static_cast<long long>(blockIdx.x) * p.rows_per_block;
+    const long long r1 = r0 + p.rows_per_block < T ? r0 + p.rows_per_block : T;
+    const __nv_bfloat16* gm = static_cast<const __nv_bfloat16*>(p.gamma);
+    float ag[VEC][8], ab[VEC][8];
+    uint4 gv[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        gv[i] = c < h ? __ldg(reinterpret_cast<const uint4*>(gm + c)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ag[i][k] = ab[i][k] = 0.0f;
+    }
+    // row r's X, dXn and residual gradient vectors, at chunk position cp
+    auto load = [&](ChunkPos cp, uint4 (&xv)[VEC], uint4 (&dv)[VEC], uint4 (&rv)[VEC]) {
+        const long long off = cp.lr * h;
+        const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x.in[cp.j]) + off;
+        const __nv_bfloat16* dy = static_cast<const __nv_bfloat16*>(p.dxn[cp.j]) + off;
+        const __nv_bfloat16* dr = static_cast<const __nv_bfloat16*>(p.dres[cp.j]) + off;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const int c = (threadIdx.x + i * LN_THREADS) * 8;
+            if (c < h) {
+                xv[i] = __ldg(reinterpret_cast<const uint4*>(x + c));
+                dv[i] = __ldg(reinterpret_cast<const uint4*>(dy + c));
+                rv[i] = __ldg(reinterpret_cast<const uint4*>(dr + c));
+            }
+        }
+    };
+    uint4 xv[VEC], dv[VEC], rv[VEC], nx[VEC], nd[VEC], nr[VEC];
+    ChunkPos cp{0, 0};
+    if (r0 < r1) {
+        cp = chunk_pos(r0, rows);
+        load(cp, xv, dv, rv);
+    }
+    for (long long r = r0; r < r1; ++r) {
+        const ChunkPos cn = chunk_advance(cp, 1, rows);
+        if (r + 1 < r1) load(cn, nx, nd, nr);
+        const float mean = __ldg(p.mean + r), rs = __ldg(p.rstd + r);
+        const float nmr = -mean * rs;  // xhat = x * rstd - mean * rstd
+        float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            if ((threadIdx.x + i * LN_THREADS) * 8 < h) {
+                float xf[8], df[8], gf[8];
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
+                unpack8(gv[i], gf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float xh = fmaf(xf[k], rs, nmr);
+                    const float g = df[k] * gf[k];
+                    sg += g;
+                    sgx = fmaf(g, xh, sgx);
+                    ag[i][k] = fmaf(df[k], xh, ag[i][k]);
+                    ab[i][k] += df[k];
+                }
+            }
+        }
+        const float2 sums = block_sum2_1bar(sg, sgx, red, static_cast<int>((r - r0) & 1));
+        // dX = rstd * g - rstd * mean(g) - xhat * rstd * mean(g * xhat) + dres
+        //    = rstd * g + c3 * x + (c4 + dres)
+        const float c2 = -rs * (sums.y / static_cast<float>(h));
+        const float c3 = c2 * rs;
+        const float c4 = fmaf(c2, nmr, -rs * (sums.x / static_cast<float>(h)));
+        __nv_bfloat16* dx = static_cast<__nv_bfloat16*>(p.dx[cp.j]) + cp.lr * h;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const int c = (threadIdx.x + i * LN_THREADS) * 8;
+            if (c < h) {
+                float xf[8], df[8], gf[8], rf[8], o[8];
+                unpack8(xv[i], xf);
+                unpack8(dv[i], df);
+                unpack8(gv[i], gf);
+                unpack8(rv[i], rf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    o[k] = fmaf(rs, df[k] * gf[k], fmaf(c3, xf[k], rf[k] + c4));
+                *reinterpret_cast<uint4*>(dx + c) = pack8(o);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            xv[i] = nx[i];
+            dv[i] = nd[i];
+            rv[i] = nr[i];
+        }
+        cp = cn;
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const int c = (threadIdx.x + i * LN_THREADS) * 8;
+        if (c < h) {
+            float* pg = p.part + (static_cast<size_t>(blockIdx.x) * 2) * h + c;
+            float* pb = pg + h;
+            *reinterpret_cast<float4*>(pg) = make_float4(ag[i][0], ag[i][1], ag[i][2], ag[i][3]);
+            *reinterpret_cast<float4*>(pg + 4) = make_float4(ag[i][4], ag[i][5], ag[i][6], ag[i][7]);
+            *reinterpret_cast<float4*>(pb) = make_float4(ab[i][0], ab[i][1], ab[i][2], ab[i][3]);
+            *reinterpret_cast<float4*>(pb + 4) = make_float4(ab[i][4], ab[i][5], ab[i][6], ab[i][7]);
         }
     }
 }
@@ -506,14 +644,24 @@ cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T,
 
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st) {
+    if (ln_backward_fused(p.h)) {
+        // dX and the partial sums in one pass over row blocks, then the finish
+        const unsigned grid = static_cast<unsigned>(splits);
+        if (p.h <= LN_THREADS * 8)
+            ln_backward_fused_kernel<1><<<grid, LN_THREADS, 0, st>>>(p, T);
+        else
+            ln_backward_fused_kernel<2><<<grid, LN_THREADS, 0, st>>>(p, T);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_colsum_f32_pair(p.part, splits, 2LL * p.h, p.h, dgamma, dbeta, st);
+    }
     if (T > 0) {
         const unsigned grid = static_cast<unsigned>(T);
-        switch (ln_vec(p.h)) {
-            case 1: ln_dx_kernel<1><<<grid, LN_THREADS, 0, st>>>(p); break;
-            case 2: ln_dx_kernel<2><<<grid, LN_THREADS, 0, st>>>(p); break;
-            case 4: ln_dx_kernel<4><<<grid, LN_THREADS, 0, st>>>(p); break;
-            default: ln_dx_kernel<8><<<grid, LN_THREADS, 0, st>>>(p); break;
-        }
+        // rows wider than LN_WARP_MAX_H: four or eight vectors per thread
+        if (ln_vec(p.h) <= 4)
+            ln_dx_kernel<4><<<grid, LN_THREADS, 0, st>>>(p);
+        else
+            ln_dx_kernel<8><<<grid, LN_THREADS, 0, st>>>(p);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -522,9 +670,7 @@ cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int split
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // dgamma = sum of part[s][0][:], dbeta = sum of part[s][1][:] over the splits
-    e = launch_colsum_f32(p.part, splits, 2LL * p.h, p.h, dgamma, st);
-    if (e != cudaSuccess) return e;
-    return launch_colsum_f32(p.part + p.h, splits, 2LL * p.h, p.h, dbeta, st);
+    return launch_colsum_f32_pair(p.part, splits, 2LL * p.h, p.h, dgamma, dbeta, st);
 }
 
 }  // namespace tpmlp

@@ -7,9 +7,12 @@
 //   dropout_backward: dZ = keep ? dOut / (1 - p) : 0 (the keep bits the
 //                     forward pass stored) and the column sums of dZ (db2)
 //   ln_backward:      dX = rstd * (g - mean(g) - xhat * mean(g * xhat)) + dOut,
-//                     g = dXn * gamma (one CTA per token row), then dgamma =
-//                     sum dXn * xhat and dbeta = sum dXn as column sums over
-//                     row splits, added in split order (no atomics anywhere).
+//                     g = dXn * gamma, dgamma = sum dXn * xhat and dbeta =
+//                     sum dXn.  Rows of at most 4096 elements: one pass over
+//                     blocks of token rows gives dX and per-block partial
+//                     sums; wider rows: one CTA per token row for dX, then
+//                     the column sums over row splits.  Either way the
+//                     partials are added in a fixed order (no atomics anywhere).
 // All three are bound by HBM traffic.
 #pragma once
 
@@ -72,15 +75,28 @@ struct LnBackwardParams {
 };
 
 constexpr int LN_MAX_SPLITS = 64;
+constexpr int LN_FUSED_MAX_BLOCKS = 512;
 
-// Bytes of partial sums the dgamma / dbeta pass needs.
+// Rows of at most LN_WARP_MAX_H elements take the fused LayerNorm backward:
+// dX and the dgamma / dbeta partial sums in one pass over row blocks.
+inline bool ln_backward_fused(long long h) { return h <= LN_WARP_MAX_H; }
+
+// Bytes of partial sums the dgamma / dbeta sums need.
 inline size_t ln_partial_bytes(long long h) {
-    return static_cast<size_t>(LN_MAX_SPLITS) * 2 * static_cast<size_t>(h) * sizeof(float);
+    const size_t splits = ln_backward_fused(h) ? LN_FUSED_MAX_BLOCKS : LN_MAX_SPLITS;
+    return splits * 2 * static_cast<size_t>(h) * sizeof(float);
 }
-// Row splits of the dgamma / dbeta pass: enough 64-column CTAs to cover the
+// Row splits of the dgamma / dbeta sums.  Fused pass: one block of rows per
+// CTA, two CTAs per SM.  Separate pass: enough 64-column CTAs to cover the
 // GPU about sixteen times (many short CTAs, so the last to start ends soon
 // after the rest), at least 128 rows per split.
 inline int ln_param_splits(long long T, long long h, int sm_count) {
+    if (ln_backward_fused(h)) {
+        long long b = 2LL * sm_count;
+        if (b > LN_FUSED_MAX_BLOCKS) b = LN_FUSED_MAX_BLOCKS;
+        if (b > T) b = T;
+        return static_cast<int>(b < 1 ? 1 : b);
+    }
     const long long strips = (h + 63) / 64;
     long long s = (16LL * sm_count + strips - 1) / strips;
     const long long by_rows = T / 128 > 0 ? T / 128 : 1;
@@ -88,14 +104,18 @@ inline int ln_param_splits(long long T, long long h, int sm_count) {
     if (s > LN_MAX_SPLITS) s = LN_MAX_SPLITS;
     return static_cast<int>(s < 1 ? 1 : s);
 }
+// Kernel launches of the LayerNorm backward.
+inline int ln_backward_launches(long long h) { return ln_backward_fused(h) ? 2 : 3; }
 
 cudaError_t launch_ln_forward(const LnForwardParams& p, long long T, cudaStream_t st);
 // Two launches: dZ with its per-split column sums, then db2 = their
 // fixed-order sum.
 cudaError_t launch_dropout_backward(const DropoutBackwardParams& p, long long T, float* db2,
                                     cudaStream_t st);
-// Four launches: dX per token row, the dgamma / dbeta partial column sums
-// over `splits` row splits, and their fixed-order finish (one per output).
+// ln_backward_launches(h) launches: dX with the dgamma / dbeta partial sums
+// over `splits` row blocks (one pass for rows of at most LN_WARP_MAX_H
+// elements, a dX pass and a partial-sum pass for wider rows), then one
+// fixed-order finish for both outputs.
 cudaError_t launch_ln_backward(const LnBackwardParams& p, long long T, int splits, float* dgamma,
                                float* dbeta, cudaStream_t st);
 

@@ -239,7 +239,7 @@ TPMLP_API tpmlp_status tpmlp_sp_backward(const tpmlp_dims* dims, const tpmlp_sp_
     lb.h = s.h;
     const int splits = ln_param_splits(s.T, s.h, dev->sm_count);
     lb.rows_per_block = (s.T + splits - 1) / splits;
-    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_BWD, 4, st, [&] {
+    TPMLP_CUDA(timed(TPMLP_KERNEL_LAYERNORM_BWD, ln_backward_launches(s.h), st, [&] {
         return launch_ln_backward(lb, s.T, splits, static_cast<float*>(dgamma),
                                   static_cast<float*>(dbeta), st);
     }));
