@@ -120,9 +120,9 @@ __global__ void colsum_finish_kernel(const float* __restrict__ partial, int spli
 }
 
 // CTA = 16 column quads (64 columns) x 16 row lanes; lane r sums rows r,
-// r + 16, ... of its four columns with 16-byte loads, then the 16 lanes are
-// combined in a fixed order.  Column c < split goes to out0[c], the others to
-// out1[c - split].
+// r + 16, ... of its four columns with 16-byte loads (eight in flight, added
+// in row order), then the 16 lanes are combined in a fixed order.  Column
+// c < split goes to out0[c], the others to out1[c - split].
 __global__ void __launch_bounds__(256) colsum_f32_kernel(const float* __restrict__ part,
                                                          long long rows, long long ld,
                                                          long long ncols, long long split,
@@ -134,13 +134,22 @@ __global__ void __launch_bounds__(256) colsum_f32_kernel(const float* __restrict
     const long long c = (static_cast<long long>(blockIdx.x) * 16 + quad) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (c < ncols) {
-        for (long long r = lane_r; r < rows; r += 16) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(part + r * ld + c));
+        auto add = [&](const float4& v) {
             acc.x += v.x;
             acc.y += v.y;
             acc.z += v.z;
             acc.w += v.w;
+        };
+        long long r = lane_r;
+        for (; r + 7 * 16 < rows; r += 8 * 16) {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = __ldg(reinterpret_cast<const float4*>(part + (r + 16 * k) * ld + c));
+#pragma unroll
+            for (int k = 0; k < 8; ++k) add(v[k]);
         }
+        for (; r < rows; r += 16) add(__ldg(reinterpret_cast<const float4*>(part + r * ld + c)));
     }
     red[lane_r][quad] = acc;
     __syncthreads();
