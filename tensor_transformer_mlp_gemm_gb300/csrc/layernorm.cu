@@ -1,13 +1,15 @@
 // layernorm.cu -- LayerNorm forward/backward and dropout backward of the
 // sequence-parallel sublayer (see layernorm.cuh).  The forward pass runs one
 // warp per token row for rows of up to 4096 elements and one CTA of 256
-// threads per row beyond that, as does the dX pass of the backward; each
-// thread holds its vectors of the row in registers, so every input is read
-// once and every output written once.  dgamma and dbeta come from a separate
-// column-reduction pass over dXn and X.  The dropout backward reads the keep
-// bits the forward pass stored and sums dZ's columns (db2) as it goes.
-// Reductions run warp-shuffle then one warp over the partial sums, always in
-// the same order.
+// threads per row beyond that; each thread holds its vectors of the row in
+// registers, so every input is read once and every output written once.  The
+// backward pass, for rows of up to 4096 elements, walks blocks of token rows
+// with one CTA each: dX row by row and the dgamma / dbeta partial sums of its
+// columns in registers, in one pass over X, dXn and dOut.  Wider rows take a
+// dX pass (one CTA per row) and a separate column-reduction pass over dXn
+// and X.  The dropout backward reads the keep bits the forward pass stored
+// and sums dZ's columns (db2) as it goes.  Reductions run warp-shuffle then
+// over the warps' partial sums, always in the same order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
