@@ -95,6 +95,7 @@ def _run_full(w, p, seed=0):
     (256, 6144, 1024, 2, 2, 0.1),   # LayerNorm rows of 3 vectors per thread (4-vector kernels)
     (128, 16384, 512, 1, 1, 0.1),   # the widest rows the LayerNorm kernels take (h = 16384)
     (2048, 4096, 256, 2, 4, 0.1),   # fused LayerNorm backward: row blocks across chunk edges
+    (256, 3000, 512, 2, 2, 0.1),    # fused LayerNorm backward, second vector per thread partly used
     (1536, 4104, 256, 1, 3, 0.1),   # rows just above the fused backward's widest (4096)
 ])
 def test_sp_layer_full(T, h, f, t, chunks, p):
